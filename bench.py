@@ -1,0 +1,359 @@
+"""Benchmark of the GB300 fused MoE expert layer.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one full layer forward (routing, permutation + activation
+quantisation, GEMM1 + SwiGLU + requantisation, GEMM2, combine) over one batch
+of synthetic tokens, through the library's C ABI.  Inputs are resident in HBM
+when the timed region starts; the timed region is bracketed by a barrier and
+torch.cuda.synchronize() on both sides and timed with CUDA events on the
+launching stream.  Every step streams the weights of all touched experts
+(larger than the 129 MB L2 for every workload), so no L2 flush is needed.
+
+Multi-GPU: the layer does not shard (one GPU, no collectives), so N GPUs run
+N independent replicas under torchrun (replicas only); value is the total
+tokens of all ranks over the slowest rank's time.
+
+--impl reference times the CPU oracle (the only reference implementation this
+project has) on the host cores, each step a bounded sample of the workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = "bf16"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=0, help="0: enough for ~3 s of timed work")
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--tokens", type=int, default=0, help="override T (decode sweep)")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def workload_spec(args):
+    s = workloads.spec(args.workload)
+    if args.tokens:
+        s["T"] = args.tokens
+    return s
+
+
+def describe(s):
+    return "%s: T=%d H=%d I=%d E=%d top-%d %s%s, logits %s" % (
+        s["name"], s["T"], s["H"], s["I"], s["E"], s["K"], s["fmt"],
+        (", clamp %g" % s["clamp"]) if s["clamp"] else "", s["logits"])
+
+
+def dtype_of(s):
+    return {"bf16": "bf16", "mxfp8": "e4m3 (mxfp8)", "nvfp4": "e2m1 (nvfp4)"}[s["fmt"]]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- roofline
+def algorithmic_bytes(s, counts):
+    """Bytes one launch of each GEMM must move at least: the touched experts'
+    weights (codes + block scales) once, its activation input and its output.
+    Returns dict kernel -> bytes, and the number of touched experts."""
+    H, I, fmt = s["H"], s["I"], s["fmt"]
+    touched = int((counts > 0).sum())
+    R = int(counts.sum())
+    if fmt == "nvfp4":
+        wb = lambda n, k: n * k // 2 + n * k // 16          # noqa: E731
+        ab = lambda k: k // 2 + k // 16                     # noqa: E731
+    elif fmt == "mxfp8":
+        wb = lambda n, k: n * k + n * k // 32               # noqa: E731
+        ab = lambda k: k + k // 32                          # noqa: E731
+    else:
+        wb = lambda n, k: 2 * n * k                         # noqa: E731
+        ab = lambda k: 2 * k                                # noqa: E731
+    g1 = touched * wb(2 * I, H) + R * ab(H) + R * ab(I)
+    g2 = touched * wb(H, I) + R * ab(I) + R * 2 * H
+    return {"gemm1_swiglu": g1, "gemm2": g2}, touched
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import moe_expert_layer_histogram_gb300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    s = workload_spec(args)
+    T = s["T"]
+
+    case = workloads.make_case(s, seed=0, device=dev)
+    layer = moe.MoELayer(T, s["H"], s["I"], s["E"], s["K"], s["fmt"], s["clamp"])
+    layer.prepare_weights(case["weights"])
+    torch.cuda.synchronize()
+    del case["weights"]
+    torch.cuda.empty_cache()
+    hidden, logits = case["hidden"], case["logits"]
+    out = torch.empty_like(hidden)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 3)):
+        layer.forward(hidden, logits, out=out)
+    torch.cuda.synchronize()
+    _, _, off, _ = layer.routing()
+    counts = np.diff(off.cpu().numpy())
+    st = layer.status()
+    if st != 0:
+        raise RuntimeError("device status %d after warm-up" % st)
+
+    # step count: ~3 s of timed work unless given
+    t0 = time.perf_counter()
+    for _ in range(5):
+        layer.forward(hidden, logits, out=out)
+    torch.cuda.synchronize()
+    per = (time.perf_counter() - t0) / 5
+    steps = args.steps or int(min(20000, max(20, 3.0 / max(per, 1e-6))))
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.5)
+    moe.moe_timing_start(layer.handle, steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        moe.moe_forward(layer.handle, hidden, logits, out, T, stream.cuda_stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    kern_ms, nrec = moe.moe_timing_stop(layer.handle)
+    clocks = sampler.stop()
+    launches = moe.moe_last_launch_count(layer.handle) * steps
+    st = layer.status()
+    if st != 0:
+        raise RuntimeError("device status %d after timed region" % st)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    value = T * steps * world / (elapsed_ms / 1e3)
+
+    # roofline of the dominant kernel
+    alg, touched = algorithmic_bytes(s, counts)
+    dom = max(("gemm1_swiglu", "gemm2"), key=lambda k: kern_ms[k])
+    avg_ms = kern_ms[dom] / max(nrec, 1)
+    peak, peak_src = measured_peaks()
+    achieved = alg[dom] / (avg_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+            "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": None, "algorithmic_bytes": alg[dom], "avg_launch_us": round(avg_ms * 1e3, 2)}
+    layer_bytes = alg["gemm1_swiglu"] + alg["gemm2"]
+    ms_step = elapsed_ms / steps
+
+    # end to end: host buffers through the C ABI, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hid_h = hidden.cpu().pin_memory()
+        lg_h = logits.cpu().pin_memory()
+        out_h = torch.empty_like(hid_h).pin_memory()
+        for _ in range(3):
+            moe.moe_forward_host(layer.handle, hid_h, lg_h, out_h, T, stream.cuda_stream)
+        e_steps = max(10, min(steps, 2000))
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            moe.moe_forward_host(layer.handle, hid_h, lg_h, out_h, T, stream.cuda_stream)
+        e_s = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_s = float(t.item())
+        e2e = {"value": round(T * e_steps * world / e_s, 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * s["H"] * 2 + T * s["E"] * 4,
+               "d2h_bytes_per_step": T * s["H"] * 2,
+               "ms_per_step": round(e_s / e_steps * 1e3, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(s, sample_tokens=cpu_sample_tokens(s))
+
+    layer.close()
+    if rank == 0:
+        line = {
+            "metric": "MoE-layer tokens/s at 1 GB300 (" + s["name"] + ")",
+            "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": dtype_of(s), "data": "synthetic (seeded; weights drawn and quantised on device)",
+            "config": {"workload": describe(s), "T": T, "H": s["H"], "I": s["I"], "E": s["E"],
+                       "top_k": s["K"], "format": s["fmt"], "clamp": s["clamp"],
+                       "touched_experts": touched, "max_rows_per_expert": int(counts.max()),
+                       "empty_experts": int((counts == 0).sum()),
+                       "l2": "no flush: every step streams %.2f GB of touched-expert weights, "
+                             "larger than the 129 MB L2" % (layer_bytes / 1e9),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roof,
+            "layer_hbm_frac": round(layer_bytes / (ms_step / 1e3) / 1e9 / peak, 4),
+            "kernels_us": {k: round(v / max(nrec, 1) * 1e3, 2) for k, v in kern_ms.items()},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- oracle arm
+def cpu_sample_tokens(s):
+    """Tokens of the workload the oracle runs for its bounded sample (about
+    10-30 s of CPU work on the host cores)."""
+    per_tok = s["K"] * 3 * s["H"] * s["I"]
+    return int(max(1, min(s["T"], 3e10 // max(per_tok, 1) // 4)))
+
+
+def cpu_baseline(s, sample_tokens):
+    import oracle
+    case = workloads.make_case(s, T=sample_tokens, seed=0, device="cpu")
+    npc = workloads.to_numpy_case(case)
+    cfg = dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"])
+    t0 = time.perf_counter()
+    oracle.forward(cfg, npc["weights"], npc["hidden"], npc["logits"])
+    dt = time.perf_counter() - t0
+    return {"value": round(sample_tokens / dt, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d tokens of the same workload (same seed, weights drawn on the "
+                      "host), one oracle forward, %.1f s" % (sample_tokens, s["T"], dt)}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    s = workload_spec(args)
+    n = max(1, min(s["T"], cpu_sample_tokens(s) // 4))
+    case = workloads.make_case(s, T=n, seed=0, device="cpu")
+    npc = workloads.to_numpy_case(case)
+    cfg = dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"])
+    steps = args.steps or 3
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle.forward(cfg, npc["weights"], npc["hidden"], npc["logits"])
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.forward(cfg, npc["weights"], npc["hidden"], npc["logits"])
+    dt = time.perf_counter() - t0
+    value = n * steps / dt
+    line = {"impl": "reference", "metric": "MoE-layer tokens/s at 1 GB300 (" + s["name"] + ")",
+            "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+            "warmup": min(args.warmup, 1), "ms_per_step": round(dt / steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": dtype_of(s), "data": "synthetic (seeded)",
+            "config": {"workload": describe(s), "T": s["T"]},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s",
+                             "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": "%d of %d tokens per step" % (n, s["T"])},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

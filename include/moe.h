@@ -1,0 +1,181 @@
+/*
+ * moe.h -- C ABI of the GB300 fused Mixture-of-Experts expert layer.
+ *
+ * One layer computes, for T tokens with hidden size H, E experts of
+ * intermediate size I and top-k K:
+ *   1. routing: per token, the K largest router logits (value descending,
+ *      lower expert index first on ties) and a softmax over those K;
+ *   2. permutation: a stable histogram / scan / scatter of the T*K
+ *      (token, k) slots into expert-contiguous order (per-expert offsets);
+ *   3. the gate/up (W13) grouped GEMM, 4. SwiGLU with an optional symmetric
+ *      gate/up clamp, fused with re-quantisation of its output,
+ *   5. the down (W2) grouped GEMM, 6. the routing-weighted top-k combine
+ *      back to token order.
+ * "One call does routing, W1 GEMM, SwiGLU, W2 GEMM and the reduction; BF16
+ * hidden states go in and are quantised inside the kernel" -- PR #40082
+ * report (Integrate flashinfer b12x MoE and FP4 GEMM kernels for SM120/121),
+ * sec. 实现拆解 item 1; the optional gate/up clamp is resolve_gate_up_clamp
+ * in "FlashInfer CuTeDSL MegaMoE kernel-drop update workflow", sec. 三.
+ *
+ * Weight formats (canonical inputs of moe_prepare_weights):
+ *   MOE_FMT_BF16 : bf16 weights.
+ *   MOE_FMT_MXFP8: e4m3 codes with one e8m0 scale per 32 elements along the
+ *                  reduction dimension (mxfp8_quantize_per_block_32, same
+ *                  workflow page, sec. 三).  Activations are quantised the
+ *                  same way inside the layer (OCP MX shared exponent).
+ *   MOE_FMT_NVFP4: e2m1 codes (two per byte, element 2j in the low nibble)
+ *                  with one e4m3 scale per 16 elements and one fp32 global
+ *                  scale per expert (nvfp4_quantize_per_block_16, sec. 三).
+ *                  moe_prepare_weights folds the global scale into the block
+ *                  scales (block_scale * global_scale re-cast to e4m3) so the
+ *                  GEMMs run with alpha = 1, and activations are quantised
+ *                  dynamically per 16-block with global scale 1 (PR #40082
+ *                  report, sec. 关键源码片段, process_weights_after_loading).
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" point to memory on the handle's CUDA device;
+ *     "host" pointers to host memory (pinned memory makes copies faster).
+ *     The caller owns every buffer it passes; the library never frees them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it; calls return before
+ *     the GPU finishes unless stated otherwise.
+ *   - Every function returns a moe_status; MOE_OK is 0.  Argument errors
+ *     are detected on the host before anything is enqueued.
+ *   - Not thread-safe per handle: one host thread at a time per moe_layer.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* NULL handle/pointer, T out of range ...   */
+    MOE_ERR_UNSUPPORTED = 2,    /* shape/format this build does not run      */
+    MOE_ERR_NO_WEIGHTS = 3,     /* moe_forward before moe_prepare_weights    */
+    MOE_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed         */
+    MOE_ERR_OOM = 5,            /* device allocation failed                  */
+    MOE_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up a bounded wait           */
+    MOE_ERR_NO_DEVICE = 7       /* no sm_103-class GPU / kernel image        */
+} moe_status;
+
+typedef enum { MOE_FMT_BF16 = 0, MOE_FMT_MXFP8 = 1, MOE_FMT_NVFP4 = 2 } moe_format;
+
+typedef struct {
+    int max_tokens;    /* T_max: largest T any forward will use (>= 1)       */
+    int hidden;        /* H: multiple of 128 (NVFP4: of 256)                 */
+    int inter;         /* I: multiple of 128 (NVFP4: of 256)                 */
+    int num_experts;   /* E: 1..512                                          */
+    int top_k;         /* K: 1..min(E, 16)                                   */
+    int format;        /* moe_format                                         */
+    float clamp_limit; /* L > 0 and finite: clamp gate and up to [-L, L]
+                          before silu(gate)*up; otherwise no clamp          */
+} moe_config;
+
+typedef struct moe_layer moe_layer;   /* opaque */
+
+/* Create a layer on the current CUDA device.  Validates `cfg` and allocates
+ * every device buffer a forward of up to cfg->max_tokens tokens needs
+ * (weights, routing tables, permuted activations, intermediates), so that
+ * moe_forward never allocates.  *out receives the handle (NULL on error).
+ * Errors: MOE_ERR_INVALID_ARG (NULL args), MOE_ERR_UNSUPPORTED (shape),
+ * MOE_ERR_NO_DEVICE, MOE_ERR_OOM (nothing leaks), MOE_ERR_CUDA.            */
+moe_status moe_create(const moe_config *cfg, moe_layer **out);
+
+/* Copy the canonical weights into the layer's own buffers and transform them
+ * into the kernels' layout (untimed set-up, enqueued on `stream`; returns
+ * after enqueueing, the caller may free its buffers once `stream` has
+ * finished).  All pointers are device pointers, row-major, reduction
+ * dimension contiguous; W13 rows 0..I-1 are the gate projection and rows
+ * I..2I-1 the up projection:
+ *   BF16 : w13 bf16 [E, 2I, H];  w2 bf16 [E, H, I];  *_sf, *_gs unused.
+ *   MXFP8: w13 e4m3 [E, 2I, H], w13_sf e8m0 [E, 2I, H/32];
+ *          w2  e4m3 [E, H, I],  w2_sf  e8m0 [E, H, I/32];  *_gs unused.
+ *   NVFP4: w13 u8 [E, 2I, H/2], w13_sf e4m3 [E, 2I, H/16], w13_gs f32 [E];
+ *          w2  u8 [E, H, I/2],  w2_sf  e4m3 [E, H, I/16],  w2_gs  f32 [E].
+ * NVFP4 block scales are multiplied by the expert's global scale and re-cast
+ * to e4m3 (the global scale becomes 1); scales are re-laid out in 128-row x
+ * 4-block tiles for the tensor cores.  Errors: MOE_ERR_INVALID_ARG when a
+ * pointer the format needs is NULL; MOE_ERR_CUDA.                          */
+moe_status moe_prepare_weights(moe_layer *layer,
+                               const void *w13, const void *w13_sf,
+                               const float *w13_gs,
+                               const void *w2, const void *w2_sf,
+                               const float *w2_gs, void *stream);
+
+/* The layer forward.  hidden: device bf16 [T, H]; router_logits: device f32
+ * [T, E]; out: device bf16 [T, H], written in place (never re-bound or
+ * reallocated).  0 <= T <= max_tokens; T == 0 is a no-op returning MOE_OK.
+ * Asynchronous on `stream`, allocates nothing, never synchronises the host.
+ * Results of a later moe_debug_* call describe the latest forward.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_NO_WEIGHTS, MOE_ERR_CUDA (launch).
+ * A kernel that gives up a bounded wait records MOE_ERR_DEVICE_TIMEOUT for
+ * moe_get_status.                                                          */
+moe_status moe_forward(moe_layer *layer, const void *hidden,
+                       const float *router_logits, void *out, int T,
+                       void *stream);
+
+/* Same as moe_forward with HOST buffers: copies hidden [T,H] bf16 and
+ * router_logits [T,E] f32 to the device, runs the layer and copies out
+ * [T,H] bf16 back, all on `stream`; returns once `stream` has finished
+ * (synchronises it).  Errors as moe_forward.                               */
+moe_status moe_forward_host(moe_layer *layer, const void *hidden_host,
+                            const float *router_logits_host, void *out_host,
+                            int T, void *stream);
+
+/* Inspection of the latest forward (tests): device destinations, any may be
+ * NULL.  topk_ids int32 [T,K], topk_w f32 [T,K], offsets int32 [E+1]
+ * (offsets[e] = first permuted row of expert e, offsets[E] = T*K),
+ * perm int32 [T*K] (permuted row -> slot t*K+k).  Enqueued on `stream`.   */
+moe_status moe_debug_routing(moe_layer *layer, int32_t *topk_ids,
+                             float *topk_w, int32_t *offsets, int32_t *perm,
+                             void *stream);
+
+/* GEMM1 input quantisation of the latest forward, per token, canonical
+ * layout: codes [T, H/2] (NVFP4) or [T, H] (MXFP8), scales [T, H/16] or
+ * [T, H/32].  Device destinations.  MOE_ERR_UNSUPPORTED for BF16.         */
+moe_status moe_debug_act_quant(moe_layer *layer, uint8_t *codes,
+                               uint8_t *scales, void *stream);
+
+/* GEMM2 input (SwiGLU output after re-quantisation, dequantised to f32,
+ * [T*K, I]) and GEMM2 output (f32 of the stored bf16, [T*K, H]) of the
+ * latest forward, in permuted row order.  Device destinations, may be NULL. */
+moe_status moe_debug_intermediates(moe_layer *layer, float *h, float *y,
+                                   void *stream);
+
+/* Device-side error word of the handle: synchronises the device, returns
+ * MOE_ERR_DEVICE_TIMEOUT if any kernel gave up a bounded wait since the
+ * last call (and clears it), MOE_ERR_CUDA on a sticky CUDA error, else
+ * MOE_OK.                                                                  */
+moe_status moe_get_status(moe_layer *layer);
+
+/* Per-kernel timing (profiling).  While on, every moe_forward records a CUDA
+ * event before each of its six kernels and one after the last, for at most
+ * max_forwards forwards; the events are created here, not in the forward.
+ * moe_timing_stop waits for the recorded work, writes the summed duration
+ * of each kernel in milliseconds to kernel_ms[6] (routing, scan, scatter +
+ * activation quantisation, GEMM1 + SwiGLU, GEMM2, combine) and the number of
+ * recorded forwards to *forwards, and turns timing off.  Errors:
+ * MOE_ERR_INVALID_ARG, MOE_ERR_CUDA.                                       */
+moe_status moe_timing_start(moe_layer *layer, int max_forwards);
+moe_status moe_timing_stop(moe_layer *layer, float *kernel_ms, int *forwards);
+
+/* Number of kernel launches the latest moe_forward enqueued.              */
+int moe_last_launch_count(const moe_layer *layer);
+
+/* Static description of a status code (never NULL).                       */
+const char *moe_status_string(moe_status s);
+
+/* Free everything the handle owns.  NULL-safe.  Synchronises the device
+ * first so no enqueued work still uses the buffers.                        */
+void moe_destroy(moe_layer *layer);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

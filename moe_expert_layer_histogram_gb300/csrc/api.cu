@@ -1,0 +1,471 @@
+// api.cu -- host runtime behind the C ABI in include/moe.h.
+//
+// moe_create sizes and allocates every device buffer once for T_max tokens
+// (the reference design also sizes its workspace once, by its maximum token
+// count: MegaMoE kernel-drop workflow page, sec. 六, num_max_tokens), so a
+// forward allocates nothing and only enqueues six kernels on the caller's
+// stream: routing + histogram, scan, scatter + activation quantisation,
+// GEMM1 (+SwiGLU/requant), GEMM2, combine.  E and K are fixed at create;
+// every launch uses the handle's E (a global-vs-local expert-count mismatch
+// broke the reference integration: PR #40082 report, sec. 风险与影响 item 3).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+#include "moe.h"
+
+using namespace moe;
+
+struct moe_layer {
+  moe_config cfg;
+  int device = 0, num_sms = 0;
+  int fmt = 0, H = 0, I = 0, E = 0, K = 0, Tmax = 0;
+  int64_t Rmax = 0, Rpad = 0;
+  int NBmax = 0;
+  int xb = 0, hb = 0;                // bytes per row: GEMM1 / GEMM2 input
+  int x_tiles_k = 0, h_tiles_k = 0;  // 128x4 scale tiles per 128-row block
+  float clamp = INFINITY;
+  std::vector<void*> allocs;
+  int32_t *ids = nullptr, *blockhist = nullptr, *base = nullptr, *pbase = nullptr;
+  int32_t *offsets = nullptr, *pad_off = nullptr, *chunk_off = nullptr, *counts = nullptr;
+  int32_t *perm = nullptr, *inv = nullptr;
+  float* w = nullptr;
+  uint8_t *xq = nullptr, *xsf = nullptr, *hq = nullptr, *hsf = nullptr, *y = nullptr;
+  uint8_t *w13 = nullptr, *w13sf = nullptr, *w2 = nullptr, *w2sf = nullptr;
+  int* status = nullptr;
+  uint8_t *h_in = nullptr, *o_out = nullptr;
+  float* l_in = nullptr;
+  GemmMaps maps1{}, maps2{};
+  bool weights_ready = false;
+  int last_T = 0, last_launches = 0;
+  std::vector<cudaEvent_t> tev;  // per-kernel timing events, 7 per forward
+  int timing_max = 0, timing_rec = 0;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows, row_bytes], box of 128 bytes x box_rows, 128-byte
+// swizzle (the layout the MMA descriptors expect).
+bool make_map(CUtensorMap* m, void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Test hook: MOE_TEST_FAIL_ALLOC_AT=n makes the n-th device allocation of
+// moe_create fail, so tests can check that the error is reported and nothing
+// leaks, without exhausting the GPU.
+struct Allocator {
+  moe_layer* L;
+  int count = 0, fail_at = 0;
+  explicit Allocator(moe_layer* l) : L(l) {
+    const char* v = std::getenv("MOE_TEST_FAIL_ALLOC_AT");
+    fail_at = v ? std::atoi(v) : 0;
+  }
+  template <class T>
+  bool get(T** p, size_t bytes) {
+    ++count;
+    *p = nullptr;
+    if (fail_at > 0 && count == fail_at) return false;
+    void* q = nullptr;
+    if (cudaMalloc(&q, std::max<size_t>(bytes, 256)) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    L->allocs.push_back(q);
+    *p = static_cast<T*>(q);
+    return true;
+  }
+};
+
+void free_all(moe_layer* L) {
+  for (void* p : L->allocs) cudaFree(p);
+  L->allocs.clear();
+}
+
+int64_t max_chunks(const moe_layer* L, int T) {
+  const int64_t R = static_cast<int64_t>(T) * L->K;
+  return std::min<int64_t>(L->E, R) + R / kRowBlock;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case MOE_ERR_NO_WEIGHTS: return "weights not prepared";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_OOM: return "device allocation failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    case MOE_ERR_NO_DEVICE: return "no usable sm_103 device";
+  }
+  return "unknown status";
+}
+
+moe_status moe_create(const moe_config* cfg, moe_layer** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  const moe_config c = *cfg;
+  if (c.max_tokens < 1 || c.hidden < 1 || c.inter < 1 || c.num_experts < 1 || c.top_k < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (c.format < MOE_FMT_BF16 || c.format > MOE_FMT_NVFP4) return MOE_ERR_INVALID_ARG;
+  const int kq = c.format == MOE_FMT_NVFP4 ? 256 : 128;
+  if (c.hidden % kq || c.inter % kq || c.num_experts > kMaxExperts || c.top_k > kMaxTopK ||
+      c.top_k > c.num_experts)
+    return MOE_ERR_UNSUPPORTED;
+  const int64_t Rmax = static_cast<int64_t>(c.max_tokens) * c.top_k;
+  const int64_t Rpad =
+      (Rmax + static_cast<int64_t>(kRowBlock - 1) * std::min<int64_t>(c.num_experts, Rmax) +
+       kRowBlock - 1) / kRowBlock * kRowBlock;
+  if (Rpad >= (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_NO_DEVICE;
+  }
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3) return MOE_ERR_NO_DEVICE;
+  if (gemm_prepare(c.format) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_NO_DEVICE;
+  }
+  if (!encode_fn()) return MOE_ERR_NO_DEVICE;
+
+  moe_layer* L = new moe_layer;
+  L->cfg = c;
+  L->device = dev;
+  L->num_sms = sms;
+  L->fmt = c.format;
+  L->H = c.hidden;
+  L->I = c.inter;
+  L->E = c.num_experts;
+  L->K = c.top_k;
+  L->Tmax = c.max_tokens;
+  L->Rmax = Rmax;
+  L->Rpad = Rpad;
+  L->NBmax = (c.max_tokens + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
+  L->clamp = (c.clamp_limit > 0.0f && std::isfinite(c.clamp_limit)) ? c.clamp_limit : INFINITY;
+  const int H = L->H, I = L->I, E = L->E;
+  if (L->fmt == MOE_FMT_NVFP4) {
+    L->xb = H / 2; L->hb = I / 2; L->x_tiles_k = H / 64; L->h_tiles_k = I / 64;
+  } else if (L->fmt == MOE_FMT_MXFP8) {
+    L->xb = H; L->hb = I; L->x_tiles_k = H / 128; L->h_tiles_k = I / 128;
+  } else {
+    L->xb = 2 * H; L->hb = 2 * I; L->x_tiles_k = 0; L->h_tiles_k = 0;
+  }
+  const size_t rblocks = static_cast<size_t>(Rpad / kRowBlock);
+  Allocator A(L);
+  bool ok = A.get(&L->ids, Rmax * 4) && A.get(&L->w, Rmax * 4) &&
+            A.get(&L->blockhist, static_cast<size_t>(L->NBmax) * E * 4) &&
+            A.get(&L->base, static_cast<size_t>(L->NBmax) * E * 4) &&
+            A.get(&L->pbase, static_cast<size_t>(L->NBmax) * E * 4) &&
+            A.get(&L->offsets, (E + 1) * 4) && A.get(&L->pad_off, (E + 1) * 4) &&
+            A.get(&L->chunk_off, (E + 1) * 4) && A.get(&L->counts, E * 4) &&
+            A.get(&L->perm, Rmax * 4) && A.get(&L->inv, Rmax * 4) &&
+            A.get(&L->xq, static_cast<size_t>(Rpad) * L->xb) &&
+            A.get(&L->xsf, rblocks * L->x_tiles_k * 512) &&
+            A.get(&L->hq, static_cast<size_t>(Rpad) * L->hb) &&
+            A.get(&L->hsf, rblocks * L->h_tiles_k * 512) &&
+            A.get(&L->y, static_cast<size_t>(Rpad) * H * 2) &&
+            A.get(&L->w13, static_cast<size_t>(E) * 2 * I * L->xb) &&
+            A.get(&L->w13sf, static_cast<size_t>(E) * (2 * I / 128) * L->x_tiles_k * 512) &&
+            A.get(&L->w2, static_cast<size_t>(E) * H * L->hb) &&
+            A.get(&L->w2sf, static_cast<size_t>(E) * (H / 128) * L->h_tiles_k * 512) &&
+            A.get(&L->status, 16) &&
+            A.get(&L->h_in, static_cast<size_t>(L->Tmax) * H * 2) &&
+            A.get(&L->l_in, static_cast<size_t>(L->Tmax) * E * 4) &&
+            A.get(&L->o_out, static_cast<size_t>(L->Tmax) * H * 2);
+  if (!ok) {
+    free_all(L);
+    delete L;
+    return MOE_ERR_OOM;
+  }
+  // Padding rows are never written by a forward; start them at zero.
+  ok = cudaMemset(L->xq, 0, static_cast<size_t>(Rpad) * L->xb) == cudaSuccess &&
+       cudaMemset(L->hq, 0, static_cast<size_t>(Rpad) * L->hb) == cudaSuccess &&
+       cudaMemset(L->y, 0, static_cast<size_t>(Rpad) * H * 2) == cudaSuccess &&
+       cudaMemset(L->status, 0, 16) == cudaSuccess;
+  for (int i = 0; i < 4 && ok; ++i) {
+    ok = make_map(&L->maps1.a[i], L->xq, L->xb, Rpad, 16u << i) &&
+         make_map(&L->maps2.a[i], L->hq, L->hb, Rpad, 16u << i);
+  }
+  ok = ok && make_map(&L->maps1.b, L->w13, L->xb, static_cast<uint64_t>(E) * 2 * I, 128) &&
+       make_map(&L->maps2.b, L->w2, L->hb, static_cast<uint64_t>(E) * H, 128) &&
+       cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    free_all(L);
+    delete L;
+    return MOE_ERR_CUDA;
+  }
+  *out = L;
+  return MOE_OK;
+}
+
+moe_status moe_prepare_weights(moe_layer* L, const void* w13, const void* w13_sf,
+                               const float* w13_gs, const void* w2, const void* w2_sf,
+                               const float* w2_gs, void* stream) {
+  if (!L || !w13 || !w2) return MOE_ERR_INVALID_ARG;
+  if (L->fmt != MOE_FMT_BF16 && (!w13_sf || !w2_sf)) return MOE_ERR_INVALID_ARG;
+  if (L->fmt == MOE_FMT_NVFP4 && (!w13_gs || !w2_gs)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int E = L->E, H = L->H, I = L->I;
+  cudaError_t e = launch_copy_rows(static_cast<const uint8_t*>(w13), L->w13,
+                                   static_cast<int64_t>(E) * 2 * I, L->xb, 2 * I, I, s);
+  if (e == cudaSuccess)
+    e = launch_copy_rows(static_cast<const uint8_t*>(w2), L->w2, static_cast<int64_t>(E) * H,
+                         L->hb, H, 0, s);
+  if (e == cudaSuccess && L->fmt != MOE_FMT_BF16) {
+    const bool nv = L->fmt == MOE_FMT_NVFP4;
+    e = launch_sf_tiles(static_cast<const uint8_t*>(w13_sf), L->w13sf, E, 2 * I,
+                        L->x_tiles_k * 4, nv ? w13_gs : nullptr, I, s);
+    if (e == cudaSuccess)
+      e = launch_sf_tiles(static_cast<const uint8_t*>(w2_sf), L->w2sf, E, H, L->h_tiles_k * 4,
+                          nv ? w2_gs : nullptr, 0, s);
+  }
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  L->weights_ready = true;
+  return MOE_OK;
+}
+
+moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, void* out, int T,
+                       void* stream) {
+  if (!L || T < 0 || T > L->Tmax) return MOE_ERR_INVALID_ARG;
+  if (T == 0) {
+    L->last_T = 0;
+    L->last_launches = 0;
+    return MOE_OK;
+  }
+  if (!hidden || !logits || !out) return MOE_ERR_INVALID_ARG;
+  if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int E = L->E, K = L->K, H = L->H, I = L->I;
+  const int NB = (T + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
+  cudaEvent_t* ev = nullptr;
+  if (L->timing_rec < L->timing_max) ev = &L->tev[static_cast<size_t>(L->timing_rec++) * 7];
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], s);
+  };
+  mark(0);
+  cudaError_t e = launch_route_hist(logits, T, E, K, L->ids, L->w, L->blockhist, s);
+  mark(1);
+  if (e == cudaSuccess)
+    e = launch_scan(L->blockhist, NB, E, L->offsets, L->pad_off, L->chunk_off, L->counts, L->base,
+                    L->pbase, s);
+  mark(2);
+  if (e == cudaSuccess)
+    e = launch_scatter_quant(L->fmt, L->ids, T, E, K, hidden, H, L->base, L->pbase, L->perm,
+                             L->inv, L->xq, L->xsf, s);
+  mark(3);
+  const int64_t chunks = max_chunks(L, T);
+  if (e == cudaSuccess) {
+    GemmArgs a{};
+    a.chunk_off = L->chunk_off;
+    a.pad_off = L->pad_off;
+    a.counts = L->counts;
+    a.E = E;
+    a.n_tiles = I / 64;
+    a.num_kb = L->xb / 128;
+    a.b_rows_per_expert = 2 * I;
+    a.sfa = L->xsf;
+    a.sfa_tiles_k = L->x_tiles_k;
+    a.sfb = L->w13sf;
+    a.sfb_tiles_k = L->x_tiles_k;
+    a.out = L->hq;
+    a.out_ld = L->hb;
+    a.out_sf = L->hsf;
+    a.out_sf_tiles_k = L->h_tiles_k;
+    a.clamp = L->clamp;
+    a.status = L->status;
+    const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
+    e = launch_gemm(L->fmt, 1, L->maps1, a, grid, s);
+  }
+  mark(4);
+  if (e == cudaSuccess) {
+    GemmArgs a{};
+    a.chunk_off = L->chunk_off;
+    a.pad_off = L->pad_off;
+    a.counts = L->counts;
+    a.E = E;
+    a.n_tiles = H / 128;
+    a.num_kb = L->hb / 128;
+    a.b_rows_per_expert = H;
+    a.sfa = L->hsf;
+    a.sfa_tiles_k = L->h_tiles_k;
+    a.sfb = L->w2sf;
+    a.sfb_tiles_k = L->h_tiles_k;
+    a.out = L->y;
+    a.out_ld = static_cast<int64_t>(H) * 2;
+    a.out_sf = nullptr;
+    a.out_sf_tiles_k = 0;
+    a.clamp = INFINITY;
+    a.status = L->status;
+    const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
+    e = launch_gemm(L->fmt, 2, L->maps2, a, grid, s);
+  }
+  mark(5);
+  if (e == cudaSuccess) e = launch_combine(L->y, L->inv, L->w, T, K, H, out, s);
+  mark(6);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  L->last_T = T;
+  L->last_launches = 6;
+  return MOE_OK;
+}
+
+moe_status moe_forward_host(moe_layer* L, const void* hidden_host, const float* logits_host,
+                            void* out_host, int T, void* stream) {
+  if (!L || T < 0 || T > L->Tmax) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return moe_forward(L, nullptr, nullptr, nullptr, 0, stream);
+  if (!hidden_host || !logits_host || !out_host) return MOE_ERR_INVALID_ARG;
+  if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t hb = static_cast<size_t>(T) * L->H * 2, lb = static_cast<size_t>(T) * L->E * 4;
+  if (cudaMemcpyAsync(L->h_in, hidden_host, hb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(L->l_in, logits_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe_status st = moe_forward(L, L->h_in, L->l_in, L->o_out, T, stream);
+  if (st != MOE_OK) return st;
+  if (cudaMemcpyAsync(out_host, L->o_out, hb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_debug_routing(moe_layer* L, int32_t* topk_ids, float* topk_w, int32_t* offsets,
+                             int32_t* perm, void* stream) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t R = static_cast<size_t>(L->last_T) * L->K;
+  bool ok = true;
+  if (topk_ids && R) ok &= cudaMemcpyAsync(topk_ids, L->ids, R * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  if (topk_w && R) ok &= cudaMemcpyAsync(topk_w, L->w, R * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  if (offsets && R)
+    ok &= cudaMemcpyAsync(offsets, L->offsets, (L->E + 1) * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  if (perm && R) ok &= cudaMemcpyAsync(perm, L->perm, R * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  return ok ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_debug_act_quant(moe_layer* L, uint8_t* codes, uint8_t* scales, void* stream) {
+  if (!L || !codes || !scales) return MOE_ERR_INVALID_ARG;
+  if (L->fmt == MOE_FMT_BF16) return MOE_ERR_UNSUPPORTED;
+  if (L->last_T == 0) return MOE_OK;
+  return launch_debug_act(L->fmt, L->inv, L->last_T, L->K, L->H, L->xq, L->xsf, codes, scales,
+                          static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+moe_status moe_debug_intermediates(moe_layer* L, float* h, float* y, void* stream) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  const int R = L->last_T * L->K;
+  if (R == 0 || (!h && !y)) return MOE_OK;
+  return launch_debug_rows(L->fmt, L->offsets, L->pad_off, L->E, R, L->I, L->H, L->hq, L->hsf,
+                           L->y, h, y, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+moe_status moe_get_status(moe_layer* L) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  int v = 0;
+  if (cudaMemcpy(&v, L->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (v != 0) {
+    cudaMemset(L->status, 0, sizeof(int));
+    return MOE_ERR_DEVICE_TIMEOUT;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_timing_start(moe_layer* L, int max_forwards) {
+  if (!L || max_forwards < 1) return MOE_ERR_INVALID_ARG;
+  for (cudaEvent_t e : L->tev) cudaEventDestroy(e);
+  L->tev.assign(static_cast<size_t>(max_forwards) * 7, nullptr);
+  for (auto& e : L->tev)
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      cudaGetLastError();
+      for (cudaEvent_t x : L->tev)
+        if (x) cudaEventDestroy(x);
+      L->tev.clear();
+      L->timing_max = L->timing_rec = 0;
+      return MOE_ERR_CUDA;
+    }
+  L->timing_max = max_forwards;
+  L->timing_rec = 0;
+  return MOE_OK;
+}
+
+moe_status moe_timing_stop(moe_layer* L, float* kernel_ms, int* forwards) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  moe_status st = MOE_OK;
+  float sum[6] = {0, 0, 0, 0, 0, 0};
+  const int n = L->timing_rec;
+  if (n > 0 && cudaEventSynchronize(L->tev[static_cast<size_t>(n) * 7 - 1]) != cudaSuccess)
+    st = MOE_ERR_CUDA;
+  for (int f = 0; f < n && st == MOE_OK; ++f)
+    for (int k = 0; k < 6; ++k) {
+      float ms = 0.0f;
+      if (cudaEventElapsedTime(&ms, L->tev[f * 7 + k], L->tev[f * 7 + k + 1]) != cudaSuccess) {
+        st = MOE_ERR_CUDA;
+        break;
+      }
+      sum[k] += ms;
+    }
+  for (cudaEvent_t e : L->tev) cudaEventDestroy(e);
+  L->tev.clear();
+  L->timing_max = L->timing_rec = 0;
+  if (st != MOE_OK) cudaGetLastError();
+  if (kernel_ms)
+    for (int k = 0; k < 6; ++k) kernel_ms[k] = sum[k];
+  if (forwards) *forwards = n;
+  return st;
+}
+
+int moe_last_launch_count(const moe_layer* L) { return L ? L->last_launches : 0; }
+
+void moe_destroy(moe_layer* L) {
+  if (!L) return;
+  cudaDeviceSynchronize();
+  for (cudaEvent_t e : L->tev) cudaEventDestroy(e);
+  free_all(L);
+  delete L;
+}
+
+}  // extern "C"

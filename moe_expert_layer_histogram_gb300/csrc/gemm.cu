@@ -1,0 +1,425 @@
+// gemm.cu -- grouped expert GEMMs on the sm_103a tensor cores (tcgen05).
+//
+// GEMM1 (W13) and GEMM2 (W2) of the layer: for every expert e with rows
+// [pad_off[e], pad_off[e] + count[e]) of the permuted activations,
+//   C = A_rows x W_e^T   (fp32 accumulation),
+// with A and W in BF16, MXFP8 (e4m3, e8m0 per 32) or NVFP4 (e2m1, e4m3 per
+// 16, global scale folded in); the block-scaled MMA applies both operands'
+// scales.  GEMM1's epilogue applies SwiGLU with the optional gate/up clamp
+// and re-quantises the result into GEMM2's input format; GEMM2's epilogue
+// stores bf16.  ("W1 GEMM, SwiGLU, W2 GEMM" -- PR #40082 report, sec.
+// 实现拆解 item 1.)
+//
+// Structure: one persistent CTA per SM walks the device-built work list
+// (expert, 128-column weight tile, 128-row token chunk).  Warp 0 (one
+// thread) streams 128-byte K slices of the activation tile and the weight
+// tile with TMA, plus their scale tiles with bulk copies, into a 6-stage
+// shared-memory ring.  Warp 1 (one thread) owns TMEM: it copies the scale
+// tiles into TMEM (tcgen05.cp) and issues 128x128 tcgen05.mma into one of two
+// 128-column fp32 accumulators.  Warps 2-5 drain the other accumulator
+// (tcgen05.ld), run the epilogue and store.  The token tile is the MMA's M
+// (128 rows; only the chunk's real rows are loaded and stored) and the weight
+// tile its N (128), so decode-sized chunks cost no extra weight traffic.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTileBytes = 128 * 128;  // 128 rows x 128 bytes of K
+constexpr int kAccCols = 128;          // TMEM columns per accumulator
+constexpr int kSfColBase = 256;        // TMEM columns for scale tiles
+constexpr int kSfColsPerStage = 32;
+constexpr int kTmemCols = 512;
+
+template <int FMT>
+struct Fmt;
+template <>
+struct Fmt<kFmtBF16> {
+  static constexpr int kSfTiles = 0;  // scale tiles per operand per stage
+};
+template <>
+struct Fmt<kFmtMXFP8> {
+  static constexpr int kSfTiles = 1;  // 128 K elements = 4 x 32-blocks
+};
+template <>
+struct Fmt<kFmtNVFP4> {
+  static constexpr int kSfTiles = 4;  // 256 K elements = 16 x 16-blocks
+};
+
+template <int FMT>
+__host__ __device__ constexpr int stage_bytes() {
+  return 2 * kTileBytes + 2 * Fmt<FMT>::kSfTiles * 512;
+}
+
+template <int FMT>
+__host__ __device__ constexpr int smem_bytes() {
+  return 1024 + kGemmStages * stage_bytes<FMT>() + (2 * kGemmStages + 5) * 8 + 16;
+}
+
+struct Item {
+  int e, n_tile, prow0, rows;
+};
+
+// Work item -> (expert, weight tile, chunk).  Items are numbered expert-major:
+// expert e owns items [chunk_off[e] * n_tiles, chunk_off[e+1] * n_tiles).
+__device__ __forceinline__ Item map_item(const GemmArgs& a, int item) {
+  int lo = 0, hi = a.E;  // chunk_off[lo]*nt <= item < chunk_off[hi]*nt
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(a.chunk_off + mid) * a.n_tiles <= item) lo = mid; else hi = mid;
+  }
+  const int c0 = __ldg(a.chunk_off + lo);
+  const int nch = __ldg(a.chunk_off + lo + 1) - c0;
+  const int local = item - c0 * a.n_tiles;
+  const int chunk = local % nch;
+  Item it;
+  it.e = lo;
+  it.n_tile = local / nch;
+  it.prow0 = __ldg(a.pad_off + lo) + chunk * kRowBlock;
+  it.rows = min(kRowBlock, __ldg(a.counts + lo) - chunk * kRowBlock);
+  return it;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u, float L) {
+  g = fminf(fmaxf(g, -L), L);
+  u = fminf(fmaxf(u, -L), L);
+  return g / (1.0f + expf(-g)) * u;
+}
+
+// ---------------------------------------------------------------- epilogues
+// Thread = accumulator row (token row `prow`); columns 0..63 hold the gate
+// and 64..127 the up projection of intermediate features 64*n_tile + j.
+template <int FMT>
+__device__ __forceinline__ void epilogue_gemm1(uint32_t taddr, bool store, int64_t prow,
+                                               int n_tile, const GemmArgs& a) {
+  if constexpr (FMT == kFmtNVFP4) {
+    uint32_t packed[8];
+    uint32_t sf4 = 0;
+#pragma unroll
+    for (int jb = 0; jb < 4; ++jb) {
+      uint32_t g[16], u[16];
+      tmem_ld16(taddr + jb * 16, g);
+      tmem_ld16(taddr + 64 + jb * 16, u);
+      tmem_ld_wait();
+      reg_fence16(g);
+      reg_fence16(u);
+      float h[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) h[i] = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]), a.clamp);
+      uint32_t c[2];
+      uint8_t sf;
+      quant_nvfp4_16(h, c, sf);
+      packed[2 * jb] = c[0];
+      packed[2 * jb + 1] = c[1];
+      sf4 |= static_cast<uint32_t>(sf) << (8 * jb);
+    }
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 32);
+      dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      *reinterpret_cast<uint32_t*>(a.out_sf + sf_tile_offset(prow, n_tile * 4, a.out_sf_tiles_k)) = sf4;
+    }
+  } else if constexpr (FMT == kFmtMXFP8) {
+#pragma unroll
+    for (int jb = 0; jb < 2; ++jb) {
+      float h[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t g[16], u[16];
+        tmem_ld16(taddr + jb * 32 + half * 16, g);
+        tmem_ld16(taddr + 64 + jb * 32 + half * 16, u);
+        tmem_ld_wait();
+        reg_fence16(g);
+        reg_fence16(u);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          h[half * 16 + i] = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]), a.clamp);
+      }
+      uint32_t c[8];
+      uint8_t sf;
+      quant_mxfp8_32(h, c, sf);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + jb * 32);
+        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+        a.out_sf[sf_tile_offset(prow, n_tile * 2 + jb, a.out_sf_tiles_k)] = sf;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int jb = 0; jb < 4; ++jb) {
+      uint32_t g[16], u[16];
+      tmem_ld16(taddr + jb * 16, g);
+      tmem_ld16(taddr + 64 + jb * 16, u);
+      tmem_ld_wait();
+      reg_fence16(g);
+      reg_fence16(u);
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float h0 = silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), a.clamp);
+        const float h1 = silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]), a.clamp);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+        o[i] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + (n_tile * 64 + jb * 16) * 2);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+  }
+}
+
+// GEMM2: 128 output features per row, stored as bf16.
+__device__ __forceinline__ void epilogue_gemm2(uint32_t taddr, bool store, int64_t prow,
+                                               int n_tile, const GemmArgs& a) {
+#pragma unroll
+  for (int jb = 0; jb < 8; ++jb) {
+    uint32_t v[16];
+    tmem_ld16(taddr + jb * 16, v);
+    tmem_ld_wait();
+    reg_fence16(v);
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + (n_tile * 128 + jb * 16) * 2);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+template <int FMT, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
+  constexpr int SFT = Fmt<FMT>::kSfTiles;
+  constexpr int SB = stage_bytes<FMT>();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGemmStages * SB);
+  uint64_t* empty = full + kGemmStages;
+  uint64_t* tfull = empty + kGemmStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drained = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGemmStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(drained, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const int total = __ldg(args.chunk_off + args.E) * args.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int i = 0; i < 4; ++i) prefetch_tmap(&maps.a[i]);
+      prefetch_tmap(&maps.b);
+      const uint64_t policy = l2_policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const Item it = map_item(args, item);
+        const int amap = it.rows <= 16 ? 0 : it.rows <= 32 ? 1 : it.rows <= 64 ? 2 : 3;
+        const uint32_t bytes = (16u << amap) * 128u + kTileBytes + 2u * SFT * 512u;
+        const int brow0 = it.e * args.b_rows_per_expert + it.n_tile * 128;
+        const uint8_t* sfa = args.sfa + static_cast<int64_t>(it.prow0 >> 7) * args.sfa_tiles_k * 512;
+        const uint8_t* sfb = args.sfb + static_cast<int64_t>(brow0 >> 7) * args.sfb_tiles_k * 512;
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sp = smem + stage * SB;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(sp, &maps.a[amap], &full[stage], kb * 128, it.prow0);
+          tma_load_2d_hint(sp + kTileBytes, &maps.b, &full[stage], kb * 128, brow0, policy);
+          if constexpr (SFT > 0) {
+            bulk_load(sp + 2 * kTileBytes, sfa + kb * SFT * 512, SFT * 512, &full[stage]);
+            bulk_load(sp + 2 * kTileBytes + SFT * 512, sfb + kb * SFT * 512, SFT * 512, &full[stage]);
+          }
+          ++issued;
+          if (++stage == kGemmStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Before leaving, make sure no copy this thread issued is still in
+      // flight (they all completed already unless the block gave up).
+      for (int back = 1; back <= kGemmStages && back <= issued; ++back) {
+        const int idx = issued - back;
+        mbar_wait(&full[idx % kGemmStages], static_cast<uint32_t>((idx / kGemmStages) & 1), nullptr);
+      }
+      if (!ok) report_status(args.status, kStatusTimeout);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t idesc;
+      if constexpr (FMT == kFmtBF16) idesc = idesc_bf16(128, 128);
+      else if constexpr (FMT == kFmtNVFP4) idesc = idesc_nvf4(128, 128);
+      else idesc = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * kAccCols;
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint8_t* sp = smem + stage * SB;
+          const uint32_t a_addr = smem_u32(sp), b_addr = smem_u32(sp + kTileBytes);
+          const uint32_t sf_col = tmem + kSfColBase + stage * kSfColsPerStage;
+          if constexpr (FMT == kFmtNVFP4) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tc_copy_sf(sf_col + j * 8, desc_sf(smem_u32(sp + 2 * kTileBytes + j * 512)));
+              tc_copy_sf(sf_col + j * 8 + 4, desc_sf(smem_u32(sp + 2 * kTileBytes + (4 + j) * 512)));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                       sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
+          } else if constexpr (FMT == kFmtMXFP8) {
+            tc_copy_sf(sf_col, desc_sf(smem_u32(sp + 2 * kTileBytes)));
+            tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sp + 2 * kTileBytes + 512)));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
+                       idesc_mxf8(128, 128, j), sf_col, sf_col + 4, (kb | j) != 0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_bf16(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                       (kb | j) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kGemmStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) tc_commit(&tfull[buf]);
+      }
+      // Every MMA this thread issued must finish before TMEM is released.
+      tc_commit(drained);
+      mbar_wait(drained, 0, nullptr);
+      if (!ok) report_status(args.status, kStatusTimeout);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int local = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++local) {
+      const Item it = map_item(args, item);
+      const int buf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      if (!mbar_wait(&tfull[buf], use & 1u, abort_flag)) {
+        if (lane == 0) report_status(args.status, kStatusTimeout);
+        break;
+      }
+      tc_fence_after();
+      const int r = q * 32 + lane;
+      if (q * 32 < it.rows) {
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols;
+        const int64_t prow = it.prow0 + r;
+        if constexpr (EPI == 1) epilogue_gemm1<FMT>(taddr, r < it.rows, prow, it.n_tile, args);
+        else epilogue_gemm2(taddr, r < it.rows, prow, it.n_tile, args);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int FMT, int EPI>
+cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t s) {
+  moe_gemm_kernel<FMT, EPI><<<grid, kGemmThreads, smem_bytes<FMT>(), s>>>(maps, args);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t prepare_one() {
+  cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<FMT, 1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<FMT>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(moe_gemm_kernel<FMT, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes<FMT>());
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int fmt) {
+  return fmt == kFmtBF16 ? smem_bytes<kFmtBF16>()
+         : fmt == kFmtMXFP8 ? smem_bytes<kFmtMXFP8>()
+                            : smem_bytes<kFmtNVFP4>();
+}
+
+cudaError_t gemm_prepare(int fmt) {
+  return fmt == kFmtBF16 ? prepare_one<kFmtBF16>()
+         : fmt == kFmtMXFP8 ? prepare_one<kFmtMXFP8>()
+                            : prepare_one<kFmtNVFP4>();
+}
+
+cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& args, int grid,
+                        cudaStream_t s) {
+  if (fmt == kFmtBF16)
+    return epi == 1 ? launch_one<kFmtBF16, 1>(maps, args, grid, s)
+                    : launch_one<kFmtBF16, 2>(maps, args, grid, s);
+  if (fmt == kFmtMXFP8)
+    return epi == 1 ? launch_one<kFmtMXFP8, 1>(maps, args, grid, s)
+                    : launch_one<kFmtMXFP8, 2>(maps, args, grid, s);
+  return epi == 1 ? launch_one<kFmtNVFP4, 1>(maps, args, grid, s)
+                  : launch_one<kFmtNVFP4, 2>(maps, args, grid, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,412 @@
+// route.cu -- routing, histogram / scan / scatter permutation with the GEMM1
+// activation quantisation fused into the scatter, the combine, and the
+// inspection kernels.
+//
+// Routing (top-k of the router logits, softmax over the selected k) and the
+// routing-weighted reduction back to token order are the first and last
+// steps of the fused layer ("routing, W1 GEMM, SwiGLU, W2 GEMM and reduction
+// in one call" -- PR #40082 report, sec. 实现拆解 item 1).  The permutation
+// is the single-GPU form of token dispatch: slots (t, k) are grouped by
+// expert with a stable counting sort (histogram per block of 64 tokens, an
+// exclusive scan over (expert, block), a scatter), and each expert's segment
+// is padded to a multiple of 128 rows so every 128-row GEMM tile and its
+// scale tiles start on a tile boundary.
+#include <cuda_bf16.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "internal.h"
+#include "quant.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// ---------------------------------------------------------------- routing
+// One warp per token.  Lane l holds logits l, l+32, ...; K rounds of a warp
+// arg-max in the total order (value descending, index ascending), then the
+// softmax of the K selected values.  Also counts, per block of 64 tokens,
+// how many slots go to each expert.
+template <int MAXJ>
+__global__ void __launch_bounds__(256) route_hist_kernel(const float* __restrict__ logits, int T,
+                                                         int E, int K, int32_t* __restrict__ ids,
+                                                         float* __restrict__ w,
+                                                         int32_t* __restrict__ blockhist) {
+  __shared__ int hist[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < kTokensPerRouteBlock; i += 8) {
+    const int t = blockIdx.x * kTokensPerRouteBlock + i;
+    if (t >= T) break;
+    const float* l = logits + static_cast<int64_t>(t) * E;
+    float v[MAXJ];
+    uint32_t avail = 0;
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = -FLT_MAX;
+      if (e < E) {
+        v[j] = __ldg(l + e);
+        avail |= 1u << j;
+      }
+    }
+    float my_v = 0.0f;
+    int my_i = 0;
+    for (int k = 0; k < K; ++k) {
+      float bv = -FLT_MAX;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j)
+        if (((avail >> j) & 1u) && (bi == INT_MAX || v[j] > bv)) {
+          bv = v[j];
+          bi = lane + 32 * j;
+        }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, off);
+        const int oi = __shfl_xor_sync(kFull, bi, off);
+        const bool take = oi != INT_MAX && (bi == INT_MAX || ov > bv || (ov == bv && oi < bi));
+        if (take) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
+      if (lane == k) {
+        my_v = bv;
+        my_i = bi;
+      }
+    }
+    const float m = __shfl_sync(kFull, my_v, 0);
+    const float ex = lane < K ? expf(my_v - m) : 0.0f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (lane < K) {
+      ids[static_cast<int64_t>(t) * K + lane] = my_i;
+      w[static_cast<int64_t>(t) * K + lane] = ex / sum;
+      atomicAdd(&hist[my_i], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    blockhist[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+// ---------------------------------------------------------------- scan
+// One block, thread e = expert.  Per-expert counts, exclusive scans of the
+// counts, of the 128-padded counts and of the 128-row chunk counts, and the
+// first (unpadded / padded) row of every (routing block, expert) pair.
+__global__ void __launch_bounds__(kMaxExperts) scan_kernel(
+    const int32_t* __restrict__ blockhist, int NB, int E, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ pad_off, int32_t* __restrict__ chunk_off, int32_t* __restrict__ counts,
+    int32_t* __restrict__ base, int32_t* __restrict__ pbase) {
+  __shared__ int wsum[3][kMaxExperts / 32];
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  int c = 0;
+  if (e < E) {
+#pragma unroll 8
+    for (int b = 0; b < NB; ++b) c += blockhist[static_cast<int64_t>(b) * E + e];
+  }
+  int v[3] = {c, (c + kRowBlock - 1) / kRowBlock * kRowBlock, (c + kRowBlock - 1) / kRowBlock};
+  int inc[3] = {v[0], v[1], v[2]};
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFull, inc[q], off);
+      if (lane >= off) inc[q] += o;
+    }
+    if (lane == 31) wsum[q][warp] = inc[q];
+  }
+  __syncthreads();
+  int ex[3];
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    int add = 0;
+    for (int w2 = 0; w2 < warp; ++w2) add += wsum[q][w2];
+    ex[q] = inc[q] - v[q] + add;
+  }
+  if (e < E) {
+    offsets[e] = ex[0];
+    pad_off[e] = ex[1];
+    chunk_off[e] = ex[2];
+    counts[e] = c;
+    if (e == E - 1) {
+      offsets[E] = ex[0] + v[0];
+      pad_off[E] = ex[1] + v[1];
+      chunk_off[E] = ex[2] + v[2];
+    }
+    int run = 0;
+    for (int b = 0; b < NB; ++b) {
+      const int64_t i = static_cast<int64_t>(b) * E + e;
+      base[i] = ex[0] + run;
+      pbase[i] = ex[1] + run;
+      run += blockhist[i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- scatter
+// Block b handles the 64 tokens of routing block b.  Warp 0 assigns, in slot
+// order, each slot its rank among the block's slots of the same expert
+// (stable), giving perm[row] = slot and the padded row of each slot.  Then
+// all warps write every token's GEMM1 input into its K padded rows:
+// BF16 copied, MXFP8 / NVFP4 quantised per block (one block per lane).
+template <int FMT>
+__global__ void __launch_bounds__(256) scatter_quant_kernel(
+    const int32_t* __restrict__ ids, int T, int E, int K, const __nv_bfloat16* __restrict__ hidden,
+    int H, const int32_t* __restrict__ base, const int32_t* __restrict__ pbase,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, uint8_t* __restrict__ xq,
+    uint8_t* __restrict__ xsf) {
+  __shared__ int cnt[kMaxExperts];
+  __shared__ int s_prow[kTokensPerRouteBlock * kMaxTopK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tok0 = blockIdx.x * kTokensPerRouteBlock;
+  const int ntok = min(kTokensPerRouteBlock, T - tok0);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  if (warp == 0) {
+    for (int i = 0; i < ntok; ++i) {
+      const int64_t s = static_cast<int64_t>(tok0 + i) * K + lane;
+      if (lane < K) {
+        const int e = ids[s];
+        const int r = cnt[e];
+        cnt[e] = r + 1;  // the K experts of one token are distinct
+        const int64_t bi = static_cast<int64_t>(blockIdx.x) * E + e;
+        perm[base[bi] + r] = static_cast<int32_t>(s);
+        const int prow = pbase[bi] + r;
+        inv[s] = prow;
+        s_prow[i * K + lane] = prow;
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
+  for (int i = warp; i < ntok; i += 8) {
+    const __nv_bfloat16* x = hidden + static_cast<int64_t>(tok0 + i) * H;
+    const int* prows = s_prow + i * K;
+    if constexpr (FMT == kFmtBF16) {
+      const uint4* src = reinterpret_cast<const uint4*>(x);
+      for (int c = lane; c < H / 8; c += 32) {
+        const uint4 val = src[c];
+        for (int k = 0; k < K; ++k)
+          reinterpret_cast<uint4*>(xq + static_cast<int64_t>(prows[k]) * H * 2)[c] = val;
+      }
+    } else if constexpr (FMT == kFmtNVFP4) {
+      const int tiles_k = H / 64;
+      for (int blk = lane; blk < H / 16; blk += 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + blk * 16);
+        float f[16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 u = src[h];
+          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+            f[8 * h + 2 * q] = p.x;
+            f[8 * h + 2 * q + 1] = p.y;
+          }
+        }
+        uint32_t codes[2];
+        uint8_t sf;
+        quant_nvfp4_16(f, codes, sf);
+        for (int k = 0; k < K; ++k) {
+          const int64_t prow = prows[k];
+          *reinterpret_cast<uint2*>(xq + prow * (H / 2) + blk * 8) = make_uint2(codes[0], codes[1]);
+          xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
+        }
+      }
+    } else {
+      const int tiles_k = H / 128;
+      for (int blk = lane; blk < H / 32; blk += 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + blk * 32);
+        float f[32];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const uint4 u = src[h];
+          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+            f[8 * h + 2 * q] = p.x;
+            f[8 * h + 2 * q + 1] = p.y;
+          }
+        }
+        uint32_t codes[8];
+        uint8_t sf;
+        quant_mxfp8_32(f, codes, sf);
+        for (int k = 0; k < K; ++k) {
+          const int64_t prow = prows[k];
+          uint4* dst = reinterpret_cast<uint4*>(xq + prow * H + blk * 32);
+          dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+          xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- combine
+// out[t] = bf16( sum_k w[t,k] * y[row(t,k)] ), fp32 accumulation in k order.
+// One block per token; each thread owns 8 consecutive columns (16-byte
+// loads and stores, coalesced along H).
+__global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ y,
+                                                      const int32_t* __restrict__ inv,
+                                                      const float* __restrict__ w, int K, int H,
+                                                      __nv_bfloat16* __restrict__ out) {
+  __shared__ int64_t s_row[kMaxTopK];
+  __shared__ float s_w[kMaxTopK];
+  const int t = blockIdx.x;
+  if (threadIdx.x < K) {
+    s_row[threadIdx.x] = inv[static_cast<int64_t>(t) * K + threadIdx.x];
+    s_w[threadIdx.x] = w[static_cast<int64_t>(t) * K + threadIdx.x];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(y + s_row[k] * H) + c);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+      const float wk = s_w[k];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+        acc[2 * q] = fmaf(wk, p.x, acc[2 * q]);
+        acc[2 * q + 1] = fmaf(wk, p.y, acc[2 * q + 1]);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      o[q] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    reinterpret_cast<uint4*>(out + static_cast<int64_t>(t) * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ---------------------------------------------------------------- inspection
+// GEMM1 input of each token back in token order, canonical layout.
+__global__ void debug_act_kernel(int fmt, const int32_t* __restrict__ inv, int K, int H,
+                                 const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xsf,
+                                 uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int t = blockIdx.x;
+  const int64_t prow = inv[static_cast<int64_t>(t) * K];
+  const int cb = fmt == kFmtNVFP4 ? H / 2 : H;
+  const int nsf = fmt == kFmtNVFP4 ? H / 16 : H / 32;
+  const int tiles_k = nsf / 4;
+  for (int i = threadIdx.x; i < cb; i += blockDim.x)
+    codes[static_cast<int64_t>(t) * cb + i] = xq[prow * cb + i];
+  for (int j = threadIdx.x; j < nsf; j += blockDim.x)
+    scales[static_cast<int64_t>(t) * nsf + j] = xsf[sf_tile_offset(prow, j, tiles_k)];
+}
+
+// GEMM2 input (dequantised) and GEMM2 output rows in unpadded row order.
+__global__ void debug_rows_kernel(int fmt, const int32_t* __restrict__ offsets,
+                                  const int32_t* __restrict__ pad_off, int E, int I, int H,
+                                  const uint8_t* __restrict__ hq, const uint8_t* __restrict__ hsf,
+                                  const __nv_bfloat16* __restrict__ y, float* __restrict__ h_out,
+                                  float* __restrict__ y_out) {
+  const int r = blockIdx.x;
+  int lo = 0, hi = E;  // offsets[lo] <= r < offsets[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (offsets[mid] <= r) lo = mid; else hi = mid;
+  }
+  const int64_t prow = pad_off[lo] + (r - offsets[lo]);
+  if (h_out) {
+    for (int i = threadIdx.x; i < I; i += blockDim.x) {
+      float v;
+      if (fmt == kFmtBF16) {
+        v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(hq)[prow * I + i]);
+      } else if (fmt == kFmtNVFP4) {
+        const uint8_t byte = hq[prow * (I / 2) + i / 2];
+        const uint8_t q = (i & 1) ? (byte >> 4) : (byte & 0xF);
+        const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+        const float e2 = (q & 8) ? -mag[q & 7] : mag[q & 7];
+        v = e2 * e4m3_to_float(hsf[sf_tile_offset(prow, i / 16, I / 64)]);
+      } else {
+        const float sc = exact_pow2(static_cast<int>(hsf[sf_tile_offset(prow, i / 32, I / 128)]) - 127);
+        v = e4m3_to_float(hq[prow * I + i]) * sc;
+      }
+      h_out[static_cast<int64_t>(r) * I + i] = v;
+    }
+  }
+  if (y_out)
+    for (int j = threadIdx.x; j < H; j += blockDim.x)
+      y_out[static_cast<int64_t>(r) * H + j] = __bfloat162float(y[prow * H + j]);
+}
+
+}  // namespace
+
+cudaError_t launch_route_hist(const float* logits, int T, int E, int K, int32_t* ids, float* w,
+                              int32_t* blockhist, cudaStream_t s) {
+  const int nb = (T + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
+  if (E <= 128)
+    route_hist_kernel<4><<<nb, 256, 0, s>>>(logits, T, E, K, ids, w, blockhist);
+  else if (E <= 256)
+    route_hist_kernel<8><<<nb, 256, 0, s>>>(logits, T, E, K, ids, w, blockhist);
+  else
+    route_hist_kernel<16><<<nb, 256, 0, s>>>(logits, T, E, K, ids, w, blockhist);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int32_t* blockhist, int NB, int E, int32_t* offsets,
+                        int32_t* pad_off, int32_t* chunk_off, int32_t* counts, int32_t* base,
+                        int32_t* pbase, cudaStream_t s) {
+  scan_kernel<<<1, kMaxExperts, 0, s>>>(blockhist, NB, E, offsets, pad_off, chunk_off, counts,
+                                        base, pbase);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int K,
+                                 const void* hidden, int H, const int32_t* base,
+                                 const int32_t* pbase, int32_t* perm, int32_t* inv, uint8_t* xq,
+                                 uint8_t* xsf, cudaStream_t s) {
+  const int nb = (T + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
+  const auto* hb = static_cast<const __nv_bfloat16*>(hidden);
+  if (fmt == kFmtBF16)
+    scatter_quant_kernel<kFmtBF16><<<nb, 256, 0, s>>>(ids, T, E, K, hb, H, base, pbase, perm, inv,
+                                                      xq, xsf);
+  else if (fmt == kFmtMXFP8)
+    scatter_quant_kernel<kFmtMXFP8><<<nb, 256, 0, s>>>(ids, T, E, K, hb, H, base, pbase, perm,
+                                                       inv, xq, xsf);
+  else
+    scatter_quant_kernel<kFmtNVFP4><<<nb, 256, 0, s>>>(ids, T, E, K, hb, H, base, pbase, perm,
+                                                       inv, xq, xsf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int K, int H,
+                           void* out, cudaStream_t s) {
+  combine_kernel<<<T, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(y), inv, w, K, H,
+                                   static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_act(int fmt, const int32_t* inv, int T, int K, int H, const uint8_t* xq,
+                             const uint8_t* xsf, uint8_t* codes, uint8_t* scales,
+                             cudaStream_t s) {
+  debug_act_kernel<<<T, 256, 0, s>>>(fmt, inv, K, H, xq, xsf, codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_rows(int fmt, const int32_t* offsets, const int32_t* pad_off, int E,
+                              int R, int I, int H, const uint8_t* hq, const uint8_t* hsf,
+                              const void* y, float* h_out, float* y_out, cudaStream_t s) {
+  debug_rows_kernel<<<R, 256, 0, s>>>(fmt, offsets, pad_off, E, I, H, hq, hsf,
+                                      static_cast<const __nv_bfloat16*>(y), h_out, y_out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,172 @@
+"""CUDA layer vs the CPU oracle on the same seeded inputs (GPU).
+
+Bit-exact: top-k ids, per-expert offsets, the permutation, and the GEMM1
+activation quantisation (codes and scales).  Within tolerance: routing
+weights (1e-6), GEMM2 input and output, and the layer output (relative L2
+<= 5e-3 for BF16 weights, <= 2e-2 for MXFP8/NVFP4).  Sizes span several GEMM
+tiles and leave ragged expert tails; edge cases: one token, forced-empty
+experts, an expert with a single row, T = max_tokens, T = 0.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests.gpu_helpers import (TOL, bf16_bits_to_f64, make_layer, rel_l2, run_gpu,
+                               run_oracle)
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    ("tiny_bf16", {}),
+    ("bf16_small", {}),
+    ("mxfp8_small", {}),
+    ("nvfp4_small", {}),
+    ("nvfp4_zipf_small", {}),
+    ("bf16_small", dict(T=300, E=4, K=2)),          # >128 rows per expert: several chunks
+    ("nvfp4_small", dict(T=200, E=3, K=2)),
+    ("mxfp8_small", dict(T=180, E=3, K=1)),
+]
+
+
+def _ids(c):
+    return c[0] + "-" + "-".join("%s%s" % kv for kv in sorted(c[1].items()))
+
+
+@pytest.mark.parametrize("name,over", CASES, ids=[_ids(c) for c in CASES])
+def test_layer_matches_oracle(name, over):
+    s = workloads.spec(name, **over)
+    case = workloads.make_case(s, seed=0)
+    ref = run_oracle(s, case, intermediates=True)
+    layer = make_layer(s, weights=case["weights"])
+    out = run_gpu(layer, case["hidden"], case["logits"])
+    ids, w, off, perm = (t.cpu().numpy() for t in layer.routing())
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert np.array_equal(ids, ref["ids"])
+    assert np.array_equal(off, ref["offsets"])
+    assert np.array_equal(perm, ref["perm"])
+    assert np.max(np.abs(w - ref["w"])) <= 1e-6
+    if s["fmt"] != "bf16":
+        codes, sf = (t.cpu().numpy() for t in layer.act_quant())
+        assert np.array_equal(sf, ref["xq_sf"]), "activation scales differ"
+        assert np.array_equal(codes, ref["xq_codes"]), "activation codes differ"
+    h, y = (t.cpu().numpy() for t in layer.intermediates())
+    assert rel_l2(h, ref["h"]) <= TOL[s["fmt"]], "GEMM2 input"
+    assert rel_l2(y, ref["y"]) <= TOL[s["fmt"]], "GEMM2 output"
+    got = out.float().cpu().numpy()
+    assert rel_l2(got, bf16_bits_to_f64(ref["out"])) <= TOL[s["fmt"]]
+    layer.close()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4"])
+def test_edge_cases_single_token_empty_and_single_row_experts(fmt):
+    name = {"bf16": "bf16_small", "mxfp8": "mxfp8_small", "nvfp4": "nvfp4_small"}[fmt]
+    s = workloads.spec(name, T=40, E=10, K=3)
+    case = workloads.make_case(s, seed=5)
+    layer = make_layer(s, weights=case["weights"])
+    # one token
+    c1 = dict(case, hidden=case["hidden"][:1], logits=case["logits"][:1])
+    ref = run_oracle(s, c1)
+    out = run_gpu(layer, c1["hidden"], c1["logits"])
+    assert np.array_equal(layer.routing()[0].cpu().numpy(), ref["ids"])
+    assert rel_l2(out.float().cpu().numpy(), bf16_bits_to_f64(ref["out"])) <= TOL[fmt]
+    # forced-empty experts 0, 4, 9 and expert 7 with exactly one row
+    lg = case["logits"].clone()
+    lg[:, [0, 4, 9]] = -1.0e4
+    lg[:, 7] = -1.0e4
+    lg[13, 7] = 1.0e4
+    ref = run_oracle(s, case, logits=lg.numpy())
+    off_ref = ref["offsets"]
+    assert off_ref[1] == off_ref[0] and off_ref[8] - off_ref[7] == 1
+    out = run_gpu(layer, case["hidden"], lg)
+    ids, w, off, perm = (t.cpu().numpy() for t in layer.routing())
+    assert np.array_equal(off, off_ref) and np.array_equal(perm, ref["perm"])
+    assert rel_l2(out.float().cpu().numpy(), bf16_bits_to_f64(ref["out"])) <= TOL[fmt]
+    assert layer.status() == 0
+    layer.close()
+
+
+def test_max_tokens_and_reuse_across_sizes():
+    s = workloads.spec("nvfp4_small", T=130, E=6, K=2)
+    case = workloads.make_case(s, seed=9)
+    layer = make_layer(s, max_tokens=130, weights=case["weights"])
+    for T in (130, 7, 64, 130):
+        c = dict(case, hidden=case["hidden"][:T], logits=case["logits"][:T])
+        ref = run_oracle(s, c)
+        out = run_gpu(layer, c["hidden"], c["logits"])
+        assert out.shape == (T, s["H"])
+        assert rel_l2(out.float().cpu().numpy(), bf16_bits_to_f64(ref["out"])) <= TOL["nvfp4"]
+    layer.close()
+
+
+def test_out_written_in_place_and_deterministic():
+    s = workloads.spec("bf16_small")
+    case = workloads.make_case(s, seed=1)
+    layer = make_layer(s, weights=case["weights"])
+    out = torch.full((s["T"], s["H"]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ptr = out.data_ptr()
+    results = []
+    for _ in range(3):
+        layer.forward(case["hidden"].cuda(), case["logits"].cuda(), out=out)
+        torch.cuda.synchronize()
+        assert out.data_ptr() == ptr
+        results.append(out.clone())
+    assert not torch.isnan(out.float()).any()
+    assert all(torch.equal(results[0], r) for r in results[1:])
+    layer.close()
+
+
+def test_forward_host_matches_device_forward():
+    from moe_expert_layer_histogram_gb300 import moe_forward_host
+    s = workloads.spec("mxfp8_small")
+    case = workloads.make_case(s, seed=2)
+    layer = make_layer(s, weights=case["weights"])
+    dev_out = run_gpu(layer, case["hidden"], case["logits"]).cpu()
+    hid = case["hidden"].contiguous().pin_memory()
+    lg = case["logits"].contiguous().pin_memory()
+    host_out = torch.empty_like(hid).pin_memory()
+    moe_forward_host(layer.handle, hid, lg, host_out, s["T"], torch.cuda.current_stream().cuda_stream)
+    assert torch.equal(host_out, dev_out)
+    layer.close()
+
+
+def test_error_codes():
+    from moe_expert_layer_histogram_gb300 import (MoEError, moe_create, moe_destroy,
+                                                  moe_forward)
+    with pytest.raises(MoEError) as e:
+        moe_create(16, 200, 128, 8, 2, "bf16")          # H not a multiple of 128
+    assert e.value.code == 2
+    with pytest.raises(MoEError) as e:
+        moe_create(16, 256, 128, 8, 9, "bf16")          # K > E
+    assert e.value.code == 2
+    with pytest.raises(MoEError) as e:
+        moe_create(0, 256, 128, 8, 2, "bf16")
+    assert e.value.code == 1
+    h = moe_create(16, 256, 128, 8, 2, "bf16")
+    x = torch.zeros(16, 256, dtype=torch.bfloat16, device="cuda")
+    lg = torch.zeros(16, 8, dtype=torch.float32, device="cuda")
+    with pytest.raises(MoEError) as e:
+        moe_forward(h, x, lg, x, 16)                    # no weights yet
+    assert e.value.code == 3
+    with pytest.raises(MoEError) as e:
+        moe_forward(h, x, lg, x, 17)                    # T > max_tokens
+    assert e.value.code == 1
+    moe_forward(h, x, lg, x, 0)                         # T == 0: no-op
+    moe_destroy(h)
+
+
+def test_allocation_failure_reports_oom_and_frees(monkeypatch):
+    from moe_expert_layer_histogram_gb300 import MoEError, moe_create, moe_destroy
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for n in (1, 5, 12):
+        monkeypatch.setenv("MOE_TEST_FAIL_ALLOC_AT", str(n))
+        with pytest.raises(MoEError) as e:
+            moe_create(512, 1024, 512, 16, 4, "nvfp4")
+        assert e.value.code == 5
+    monkeypatch.delenv("MOE_TEST_FAIL_ALLOC_AT")
+    h = moe_create(512, 1024, 512, 16, 4, "nvfp4")
+    moe_destroy(h)
+    torch.cuda.synchronize()
+    assert abs(torch.cuda.mem_get_info()[0] - free0) < (64 << 20)
