@@ -172,6 +172,14 @@ def run_ours(args):
     layer = moe.MoELayer(T, s["H"], s["I"], s["E"], s["K"], s["fmt"], s["clamp"])
     layer.prepare_weights(case["weights"])
     torch.cuda.synchronize()
+    w_sample = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle's bounded sample: the first n tokens of this very
+        # workload and the experts they touch, copied off the device
+        import oracle
+        n = cpu_sample_tokens(s)
+        ids, _ = oracle.route(case["logits"][:n].cpu().numpy(), s["K"])
+        w_sample = (n, workloads.host_weights(s, ids.reshape(-1), source=case["weights"]))
     del case["weights"]
     torch.cuda.empty_cache()
     hidden, logits = case["hidden"], case["logits"]
@@ -262,7 +270,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(s, sample_tokens=cpu_sample_tokens(s))
+        cpu = cpu_baseline(s, case, w_sample)
 
     layer.close()
     if rank == 0:
@@ -293,55 +301,82 @@ def run_ours(args):
 
 
 # ---------------------------------------------------------------- oracle arm
-def cpu_sample_tokens(s):
+def oracle_cost_core_s(s, n):
+    """Rough core-seconds of one oracle forward over n tokens: the dot
+    products plus decoding every touched expert's weights once."""
+    E, K, H, I = s["E"], s["K"], s["H"], s["I"]
+    touched = E * (1.0 - (1.0 - K / E) ** n)
+    dec = {"bf16": 1e-9, "mxfp8": 3e-9, "nvfp4": 4e-9}[s["fmt"]]
+    return n * K * 3 * H * I * 1.2e-9 + touched * 3 * H * I * dec
+
+
+def cpu_sample_tokens(s, core_seconds=20.0):
     """Tokens of the workload the oracle runs for its bounded sample (about
     10-30 s of CPU work on the host cores)."""
-    per_tok = s["K"] * 3 * s["H"] * s["I"]
-    return int(max(1, min(s["T"], 3e10 // max(per_tok, 1) // 4)))
+    n = 1
+    while n < s["T"] and oracle_cost_core_s(s, n + 1) <= core_seconds:
+        n += 1
+    return n
 
 
-def cpu_baseline(s, sample_tokens):
+def _cfg(s):
+    return dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"])
+
+
+def cpu_baseline(s, case, w_sample):
     import oracle
-    case = workloads.make_case(s, T=sample_tokens, seed=0, device="cpu")
-    npc = workloads.to_numpy_case(case)
-    cfg = dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"])
+    import torch
+    n, wh = w_sample
+    hid = case["hidden"][:n].cpu().view(torch.int16).numpy().view("uint16")
+    lg = case["logits"][:n].cpu().numpy()
     t0 = time.perf_counter()
-    oracle.forward(cfg, npc["weights"], npc["hidden"], npc["logits"])
+    oracle.forward(_cfg(s), wh, hid, lg)
     dt = time.perf_counter() - t0
-    return {"value": round(sample_tokens / dt, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": "%d of %d tokens of the same workload (same seed, weights drawn on the "
-                      "host), one oracle forward, %.1f s" % (sample_tokens, s["T"], dt)}
+            "sample": "first %d of %d tokens of the same workload and the %d experts they touch "
+                      "(weights copied from the device), one oracle forward, %.1f s wall"
+                      % (n, s["T"], len(set(oracle.route(lg, s["K"])[0].reshape(-1).tolist())), dt)}
 
 
 def run_reference(args):
+    """The oracle as it stands, timed on the host cores.  Each step is one
+    oracle forward over the first n tokens of the workload, n sized so the
+    whole --warmup/--steps run stays within a few minutes."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import oracle
+    import torch
     s = workload_spec(args)
-    n = max(1, min(s["T"], cpu_sample_tokens(s) // 4))
-    case = workloads.make_case(s, T=n, seed=0, device="cpu")
-    npc = workloads.to_numpy_case(case)
-    cfg = dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"])
     steps = args.steps or 3
-    for _ in range(max(0, min(args.warmup, 1))):
-        oracle.forward(cfg, npc["weights"], npc["hidden"], npc["logits"])
+    warm = min(args.warmup, 1)
+    budget_core_s = 120.0 * oracle.num_threads() / max(1, steps + warm)
+    n = max(1, min(cpu_sample_tokens(s, budget_core_s), s["T"]))
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    case = workloads.make_case(s, seed=0, device=dev, weights=False)
+    lg = case["logits"][:n].cpu().numpy()
+    hid = case["hidden"][:n].cpu().view(torch.int16).numpy().view("uint16")
+    ids, _ = oracle.route(lg, s["K"])
+    wh = workloads.host_weights(s, ids.reshape(-1), device=dev)
+    for _ in range(warm):
+        oracle.forward(_cfg(s), wh, hid, lg)
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle.forward(cfg, npc["weights"], npc["hidden"], npc["logits"])
+        oracle.forward(_cfg(s), wh, hid, lg)
     dt = time.perf_counter() - t0
     value = n * steps / dt
     line = {"impl": "reference", "metric": "MoE-layer tokens/s at 1 GB300 (" + s["name"] + ")",
             "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": steps,
-            "warmup": min(args.warmup, 1), "ms_per_step": round(dt / steps * 1e3, 3),
+            "warmup": warm, "ms_per_step": round(dt / steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": dtype_of(s), "data": "synthetic (seeded)",
             "config": {"workload": describe(s), "T": s["T"]},
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s",
                              "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": "%d of %d tokens per step" % (n, s["T"])},
+                             "sample": "first %d of %d tokens per step, the experts they touch"
+                                       % (n, s["T"])},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

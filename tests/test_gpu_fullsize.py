@@ -1,0 +1,73 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark times (one layer created for T tokens, one forward), on sampled
+outputs the oracle computes one token at a time (GPU).
+
+At full size the whole routing is still checked bit-exactly (top-k ids,
+per-expert offsets, the permutation); the GEMM1 activation quantisation and
+the layer output are checked on sampled tokens, the output against the
+oracle's per-token brute-force evaluation.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.gpu_helpers import TOL, bf16_bits_to_f64, cfg_of, make_layer, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+FULL = [("bf16", None), ("mxfp8_decode", None), ("nvfp4_decode", 1), ("nvfp4_decode", 8),
+        ("nvfp4_decode", 32), ("nvfp4_decode", 128), ("nvfp4_prefill", None)]
+
+
+def _sample(T, n=5, seed=0):
+    rng = np.random.default_rng(seed)
+    pick = {0, T - 1} | set(int(x) for x in rng.choice(T, size=min(T, n), replace=False))
+    return sorted(pick)
+
+
+def _check(s, case, logits_dev, layer, sample):
+    T = logits_dev.shape[0]
+    out = layer.forward(case["hidden"], logits_dev)
+    torch.cuda.synchronize()
+    ids, w, off, perm = (t.cpu().numpy() for t in layer.routing())
+    assert layer.status() == 0
+    lg = logits_dev.cpu().numpy()
+    ids_ref, w_ref = oracle.route(lg, s["K"])
+    off_ref, perm_ref, _ = oracle.permute(ids_ref, s["E"])
+    assert np.array_equal(ids, ids_ref)
+    assert np.array_equal(off, off_ref)
+    assert np.array_equal(perm, perm_ref)
+    assert np.max(np.abs(w - w_ref)) <= 1e-6
+    hid = case["hidden"].cpu().view(torch.int16).numpy().view(np.uint16)
+    if s["fmt"] != "bf16":
+        codes, sf = (t.cpu().numpy() for t in layer.act_quant())
+        x = (hid[sample].astype(np.uint32) << 16).view(np.float32)
+        rc, rs = oracle.quant_row(s["fmt"], x)
+        assert np.array_equal(codes[sample], rc) and np.array_equal(sf[sample], rs)
+    wh = workloads.host_weights(s, ids_ref[sample].reshape(-1), source=case["weights"])
+    got = out.float().cpu().numpy()[sample]
+    want = np.stack([oracle.token_forward(cfg_of(s), wh, hid[t], lg[t])[1] for t in sample])
+    assert rel_l2(got, bf16_bits_to_f64(want)) <= TOL[s["fmt"]]
+    return off
+
+
+@pytest.mark.parametrize("name,T", FULL, ids=["%s-%s" % f for f in FULL])
+def test_full_size_sampled(name, T):
+    s = workloads.spec(name, **({"T": T} if T else {}))
+    case = workloads.make_case(s, seed=0, device="cuda")
+    layer = make_layer(s, weights=case["weights"])
+    off = _check(s, case, case["logits"], layer, _sample(s["T"]))
+    counts = np.diff(off)
+    if name == "nvfp4_prefill":
+        # Zipf(1.1) popularity: strongly imbalanced load
+        assert counts.max() > 8 * max(1, np.median(counts))
+        if (counts == 0).sum() == 0:
+            # no expert went empty on its own: force the 16 least popular
+            # experts empty and check again
+            order = np.argsort(counts)[:16]
+            lg = workloads.forced_empty_logits(case["logits"], torch.as_tensor(order).cuda())
+            off2 = _check(s, case, lg, layer, _sample(s["T"], seed=1))
+            assert (np.diff(off2)[order] == 0).all()
+    layer.close()

@@ -154,53 +154,97 @@ def draw_hidden(s, T, g, device):
                        dtype=torch.float32).to(torch.bfloat16).contiguous()
 
 
-def draw_weights(s, g, device):
-    """Canonical weights: W13 [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up) and
-    W2 [E, H, I], reduction dim contiguous.  Drawn in the input-major shapes
-    [E, H, 2I] and [E, I, H] and transposed.  Quantised per expert for
-    MXFP8/NVFP4."""
+def _expert_gen(seed, which, e, device):
+    # every expert matrix has its own generator, so any subset of experts can
+    # be drawn (or re-drawn) without drawing the others
+    return _gen(seed * 1000003 + 2 * e + (1 if which == "w13" else 2), device)
+
+
+def draw_expert(s, which, e, seed, device):
+    """One expert's canonical matrix: W13_e [2I, H] or W2_e [H, I] (bf16), or
+    its quantised codes, block scales and (NVFP4) global scale."""
+    H, I, fmt = s["H"], s["I"], s["fmt"]
+    rows_in, cols_out = (H, 2 * I) if which == "w13" else (I, H)
+    std = (1.0 / math.sqrt(rows_in)) if s["wdist"] == "fan_in" else float(s["wdist"])
+    g = _expert_gen(seed, which, e, device)
+    x = (torch.randn(rows_in, cols_out, generator=g, device=device,
+                     dtype=torch.float32) * std).to(torch.bfloat16)
+    x = x.t().contiguous()                         # [N = cols_out, K = rows_in]
+    if fmt == "bf16":
+        return {which: x}
+    if fmt == "nvfp4":
+        c, f, gsc = quantize_weight_nvfp4(x)
+        return {which: c, which + "_sf": f, which + "_gs": gsc}
+    c, f = quantize_weight_mxfp8(x)
+    return {which: c, which + "_sf": f}
+
+
+def weight_shapes(s):
+    """name -> (shape, torch dtype) of the canonical weight arrays."""
     E, H, I, fmt = s["E"], s["H"], s["I"], s["fmt"]
     out = {}
-    for name, (rows_in, cols_out) in (("w13", (H, 2 * I)), ("w2", (I, H))):
-        std = (1.0 / math.sqrt(rows_in)) if s["wdist"] == "fan_in" else float(s["wdist"])
+    for which, (N, K) in (("w13", (2 * I, H)), ("w2", (H, I))):
         if fmt == "bf16":
-            w = torch.empty(E, cols_out, rows_in, dtype=torch.bfloat16, device=device)
+            out[which] = ((E, N, K), torch.bfloat16)
         elif fmt == "nvfp4":
-            w = torch.empty(E, cols_out, rows_in // 2, dtype=torch.uint8, device=device)
-            sf = torch.empty(E, cols_out, rows_in // 16, dtype=torch.uint8, device=device)
-            gs = torch.empty(E, dtype=torch.float32, device=device)
+            out[which] = ((E, N, K // 2), torch.uint8)
+            out[which + "_sf"] = ((E, N, K // 16), torch.uint8)
+            out[which + "_gs"] = ((E,), torch.float32)
         else:
-            w = torch.empty(E, cols_out, rows_in, dtype=torch.uint8, device=device)
-            sf = torch.empty(E, cols_out, rows_in // 32, dtype=torch.uint8, device=device)
-        for e in range(E):
-            x = (torch.randn(rows_in, cols_out, generator=g, device=device,
-                             dtype=torch.float32) * std).to(torch.bfloat16)
-            x = x.t().contiguous()                     # [N = cols_out, K = rows_in]
-            if fmt == "bf16":
-                w[e] = x
-            elif fmt == "nvfp4":
-                c, f, gsc = quantize_weight_nvfp4(x)
-                w[e], sf[e], gs[e] = c, f, gsc
+            out[which] = ((E, N, K), torch.uint8)
+            out[which + "_sf"] = ((E, N, K // 32), torch.uint8)
+    return out
+
+
+def draw_weights(s, seed, device):
+    """Canonical weights of all experts: W13 [E, 2I, H] (rows 0..I-1 gate,
+    I..2I-1 up) and W2 [E, H, I], reduction dim contiguous.  Each expert
+    matrix is drawn in the input-major shape ([H, 2I] / [I, H]), transposed
+    and, for MXFP8/NVFP4, quantised."""
+    out = {k: torch.empty(shape, dtype=dt, device=device)
+           for k, (shape, dt) in weight_shapes(s).items()}
+    for which in ("w13", "w2"):
+        for e in range(s["E"]):
+            for k, v in draw_expert(s, which, e, seed, device).items():
+                out[k][e] = v
+    return out
+
+
+def host_weights(s, experts, seed=0, source=None, device="cpu"):
+    """numpy weights of full shape for the oracle in which only `experts` are
+    filled (the other experts' pages are never touched, so a full-size layer
+    costs host memory only for the experts a sampled check needs).  Copies
+    from `source` (device weights of the same seed) or draws them on
+    `device` and copies them to the host."""
+    import numpy as np
+    out = {}
+    for k, (shape, dt) in weight_shapes(s).items():
+        npdt = {torch.bfloat16: np.uint16, torch.uint8: np.uint8, torch.float32: np.float32}[dt]
+        out[k] = np.zeros(shape, npdt)
+    for e in sorted(set(int(x) for x in experts)):
+        for which in ("w13", "w2"):
+            if source is not None:
+                part = {k: source[k][e] for k in source if k.startswith(which)}
             else:
-                c, f = quantize_weight_mxfp8(x)
-                w[e], sf[e] = c, f
-        out[name] = w
-        if fmt != "bf16":
-            out[name + "_sf"] = sf
-        if fmt == "nvfp4":
-            out[name + "_gs"] = gs
+                part = draw_expert(s, which, e, seed, device)
+            for k, v in part.items():
+                v = v.detach().cpu()
+                if v.dtype == torch.bfloat16:
+                    v = v.view(torch.int16)
+                out[k][e] = v.numpy().view(out[k].dtype) if v.dim() else v.item()
     return out
 
 
 def make_case(s, T=None, seed=0, device="cpu", weights=True):
-    """Draw one workload: logits, hidden, then W13, W2 (in that order)."""
+    """Draw one workload: logits then hidden from one generator, and the
+    weights from per-expert generators."""
     T = s["T"] if T is None else T
     g = _gen(seed, device)
     case = {"spec": s, "T": T}
     case["logits"] = draw_logits(s, T, g, device)
     case["hidden"] = draw_hidden(s, T, g, device)
     if weights:
-        case["weights"] = draw_weights(s, g, device)
+        case["weights"] = draw_weights(s, seed, device)
     return case
 
 
