@@ -11,11 +11,12 @@
  *      gate/up clamp, fused with re-quantisation of its output,
  *   5. the down (W2) grouped GEMM, 6. the routing-weighted top-k combine
  *      back to token order.
- * "One call does routing, W1 GEMM, SwiGLU, W2 GEMM and the reduction; BF16
- * hidden states go in and are quantised inside the kernel" -- PR #40082
- * report (Integrate flashinfer b12x MoE and FP4 GEMM kernels for SM120/121),
- * sec. 实现拆解 item 1; the optional gate/up clamp is resolve_gate_up_clamp
- * in "FlashInfer CuTeDSL MegaMoE kernel-drop update workflow", sec. 三.
+ * The b12x integration report (PR #40082 report, "Integrate flashinfer b12x
+ * MoE and FP4 GEMM kernels for SM120/121", sec. 实现拆解 item 1) describes the
+ * same sequence run by a single call that takes bf16 hidden states and
+ * quantises them itself; the optional gate/up clamp corresponds to
+ * resolve_gate_up_clamp in the MegaMoE kernel-drop workflow page
+ * ("FlashInfer CuTeDSL MegaMoE kernel-drop update workflow"), sec. 三.
  *
  * Weight formats (canonical inputs of moe_prepare_weights):
  *   MOE_FMT_BF16 : bf16 weights.

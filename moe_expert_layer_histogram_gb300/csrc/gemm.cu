@@ -7,8 +7,8 @@
 // 16, global scale folded in); the block-scaled MMA applies both operands'
 // scales.  GEMM1's epilogue applies SwiGLU with the optional gate/up clamp
 // and re-quantises the result into GEMM2's input format; GEMM2's epilogue
-// stores bf16.  ("W1 GEMM, SwiGLU, W2 GEMM" -- PR #40082 report, sec.
-// 实现拆解 item 1.)
+// stores bf16.  (The two expert GEMMs with SwiGLU between them: PR #40082
+// report, sec. 实现拆解 item 1.)
 //
 // Structure: one persistent CTA per SM walks the device-built work list
 // (expert, 128-column weight tile, 128-row token chunk).  Warp 0 (one

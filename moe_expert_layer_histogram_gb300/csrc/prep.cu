@@ -7,12 +7,12 @@
 //    halves of the same 64 intermediate features and the GEMM1 epilogue sees
 //    both in one accumulator row;
 //  - block scales are re-laid out into 128-row x 4-scale tiles for the
-//    tensor cores (the MMA scale-factor layout: "w1_sf_mma / w2_sf_mma
-//    precomputed once in process_weights_after_loading", PR #40082 report,
-//    sec. 关键源码片段);
+//    tensor cores; like the b12x integration, which converts its scales to
+//    the MMA layout once at weight-load time (PR #40082 report, sec.
+//    关键源码片段), this happens once, not per forward;
 //  - NVFP4 scales are first multiplied by the expert's fp32 global scale and
-//    re-cast to e4m3 ("block_scale.float() * weight_scale_2 ... .to(block
-//    scale dtype)", same section), so the GEMMs run with alpha = 1.
+//    the product rounded back to e4m3, after which the global scale is 1
+//    (same section), so the GEMMs run with alpha = 1.
 #include "internal.h"
 #include "quant.cuh"
 

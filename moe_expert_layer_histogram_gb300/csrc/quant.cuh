@@ -2,10 +2,10 @@
 //
 // NVFP4 (16-element blocks, e4m3 scale, activation global scale 1) and
 // MXFP8 (32-element blocks, e8m0 scale) quantisation of fp32 values, as the
-// layer applies it to its GEMM inputs ("activations quantised dynamically
-// per block inside the kernel" with the activation global scale forced to 1:
-// PR #40082 report, sec. 关键源码片段; block sizes 16 / 32 from the MegaMoE
-// kernel-drop workflow page, sec. 三, nvfp4_quantize_per_block_16 /
+// layer applies it to its GEMM inputs: dynamic per-block scales computed in
+// the kernel, with the activation global scale fixed at 1 (PR #40082 report,
+// sec. 关键源码片段); block sizes 16 / 32 from the MegaMoE kernel-drop
+// workflow page, sec. 三 (nvfp4_quantize_per_block_16 /
 // mxfp8_quantize_per_block_32).
 //   NVFP4: sf = e4m3_rn_satfinite(amax / 6); q_i = e2m1_rn_satfinite(x_i / sf)
 //          with both divisions correctly rounded; sf == 0 gives zero codes.

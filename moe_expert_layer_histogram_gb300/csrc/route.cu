@@ -4,9 +4,9 @@
 //
 // Routing (top-k of the router logits, softmax over the selected k) and the
 // routing-weighted reduction back to token order are the first and last
-// steps of the fused layer ("routing, W1 GEMM, SwiGLU, W2 GEMM and reduction
-// in one call" -- PR #40082 report, sec. 实现拆解 item 1).  The permutation
-// is the single-GPU form of token dispatch: slots (t, k) are grouped by
+// steps of the fused layer, which the b12x integration runs together with
+// both expert GEMMs in one call (PR #40082 report, sec. 实现拆解 item 1).  The
+// permutation is the single-GPU form of token dispatch: slots (t, k) are grouped by
 // expert with a stable counting sort (histogram per block of 64 tokens, an
 // exclusive scan over (expert, block), a scatter), and each expert's segment
 // is padded to a multiple of 128 rows so every 128-row GEMM tile and its

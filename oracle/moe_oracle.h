@@ -13,9 +13,9 @@
  *   clamp, re-quantisation of the GEMM2 input, per-expert W2 GEMM and the
  *   routing-weighted top-k combine.  Sources:
  *     - "PR #40082 report: Integrate flashinfer b12x MoE and FP4 GEMM kernels
- *       for SM120/121" (prhub.com.cn), sec. 实现拆解 item 1: one call does
- *       routing, W1 GEMM, SwiGLU, W2 GEMM and the reduction; BF16 hidden
- *       states go in and are quantised inside the kernel.
+ *       for SM120/121" (prhub.com.cn), sec. 实现拆解 item 1: the layer's steps
+ *       (routing, the gate/up GEMM, SwiGLU, the down GEMM, the reduction)
+ *       in one call that receives bf16 activations and quantises them.
  *     - same page, sec. 关键源码片段 (process_weights_after_loading): the
  *       per-expert fp32 global weight scale is multiplied into the block
  *       scales, the product re-cast to the block-scale type, and the global

@@ -10,8 +10,9 @@ Quantised weights are produced the way an offline quantiser (modelopt
 convention) produces a checkpoint, *before* the layer ever sees them:
   NVFP4: per expert global scale gs = amax_e / (6 * 448); per 16-block scale
          sf = e4m3(amax_b / (6 * gs)); codes q = e2m1(x / (sf * gs)).
-         ("block_scale = max_abs * w_gs / fp4_max" -- PR #40082 report, sec.
-         关键源码片段, comment in process_weights_after_loading.)
+         (the block scale is the block's largest magnitude times the global
+         quantisation scale over the largest e2m1 value, the vLLM convention
+         restated in PR #40082 report, sec. 关键源码片段.)
   MXFP8: per 32-block shared exponent X = floor(log2 amax) - 8, e8m0 scale
          X + 127, codes e4m3(x * 2^-X) (OCP MX v1.0 conversion rule).
 The element roundings use torch's float8_e4m3fn cast (round to nearest even)
