@@ -169,6 +169,28 @@ moe_status moe_timing_stop(moe_layer *layer, float *kernel_ms, int *forwards);
 /* Number of kernel launches the latest moe_forward enqueued.              */
 int moe_last_launch_count(const moe_layer *layer);
 
+/* Routing and expert permutation without any device allocation.  The pages
+ * have no counterpart of this entry point; it exists for callers that cannot
+ * call cudaMalloc -- e.g. a serving framework whose caching allocator
+ * already owns the GPU's memory, or a latency-critical caller that cannot
+ * accept the device-wide synchronisation an allocation may cause.
+ * Computes exactly what moe_forward's routing + permutation step computes
+ * (see moe_debug_routing): router_logits device f32 [T,E] in; device
+ * outputs topk_ids int32 [T,K], topk_w f32 [T,K], offsets int32 [E+1],
+ * perm int32 [T*K].  Needs no handle.  Its scratch is one fixed 256 KiB
+ * device array inside the library (held on every GPU that loads it until
+ * the process exits), which limits it to T <= 4096, E <= 512, K <= 16:
+ * larger sizes return MOE_ERR_UNSUPPORTED.  The first call on a device looks
+ * up that array's device address (make that first call before any stream
+ * capture).  All calls share the array: calls whose work overlaps on the
+ * GPU (other streams, unordered host threads) race and give wrong results.
+ * Errors: MOE_ERR_INVALID_ARG (T < 0, K > E, NULL pointer),
+ * MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.  T == 0 is a no-op.                  */
+moe_status moe_route_permute_static(const float *router_logits, int T, int E,
+                                    int K, int32_t *topk_ids, float *topk_w,
+                                    int32_t *offsets, int32_t *perm,
+                                    void *stream);
+
 /* Static description of a status code (never NULL).                       */
 const char *moe_status_string(moe_status s);
 

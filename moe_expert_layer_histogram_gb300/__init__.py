@@ -39,7 +39,7 @@ class MoEError(RuntimeError):
 EXPORTS = ("moe_create", "moe_prepare_weights", "moe_forward", "moe_forward_host",
            "moe_debug_routing", "moe_debug_act_quant", "moe_debug_intermediates",
            "moe_get_status", "moe_timing_start", "moe_timing_stop", "moe_last_launch_count",
-           "moe_status_string", "moe_destroy")
+           "moe_route_permute_static", "moe_status_string", "moe_destroy")
 
 _lib = None
 
@@ -64,6 +64,7 @@ def lib():
     L.moe_timing_start.argtypes = [vp, ci]
     L.moe_timing_stop.argtypes = [vp, vp, vp]
     L.moe_last_launch_count.argtypes = [vp]
+    L.moe_route_permute_static.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp, vp]
     L.moe_status_string.argtypes = [ci]
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_destroy.argtypes = [vp]
@@ -153,6 +154,16 @@ def moe_timing_stop(handle):
 
 def moe_last_launch_count(handle):
     return lib().moe_last_launch_count(handle)
+
+
+def moe_route_permute_static(router_logits, T, E, K, topk_ids, topk_w, offsets, perm,
+                             stream=None):
+    """Routing + expert permutation with no device allocation (for callers
+    that cannot allocate; scratch is a fixed array inside the library, so
+    T <= 4096 and concurrent calls on the GPU must not overlap)."""
+    _check(lib().moe_route_permute_static(_ptr(router_logits), int(T), int(E), int(K),
+                                          _ptr(topk_ids), _ptr(topk_w), _ptr(offsets),
+                                          _ptr(perm), stream), "moe_route_permute_static")
 
 
 def moe_destroy(handle):
