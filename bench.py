@@ -41,6 +41,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--tokens", type=int, default=0, help="override T (decode sweep)")
+    p.add_argument("--experts", type=int, default=0,
+                   help="override E (small cases for profiler captures)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -51,6 +53,8 @@ def workload_spec(args):
     s = workloads.spec(args.workload)
     if args.tokens:
         s["T"] = args.tokens
+    if args.experts:
+        s["E"] = args.experts
     return s
 
 
@@ -206,7 +210,6 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.5)
-    moe.moe_timing_start(layer.handle, steps)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -220,7 +223,6 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     elapsed_ms = ev0.elapsed_time(ev1)
-    kern_ms, nrec = moe.moe_timing_stop(layer.handle)
     clocks = sampler.stop()
     launches = moe.moe_last_launch_count(layer.handle) * steps
     st = layer.status()
@@ -231,6 +233,17 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     value = T * steps * world / (elapsed_ms / 1e3)
+
+    # per-kernel durations: a second timed pass with CUDA events recorded
+    # around every kernel (kept out of the pass above: events between kernels
+    # also stop consecutive kernels from overlapping their launch)
+    prof_steps = min(steps, 2000)
+    moe.moe_timing_start(layer.handle, prof_steps)
+    torch.cuda.synchronize()
+    for _ in range(prof_steps):
+        moe.moe_forward(layer.handle, hidden, logits, out, T, stream.cuda_stream)
+    torch.cuda.synchronize()
+    kern_ms, nrec = moe.moe_timing_stop(layer.handle)
 
     # roofline of the dominant kernel
     alg, touched = algorithmic_bytes(s, counts)
@@ -290,6 +303,8 @@ def run_ours(args):
             "roofline": roof,
             "layer_hbm_frac": round(layer_bytes / (ms_step / 1e3) / 1e9 / peak, 4),
             "kernels_us": {k: round(v / max(nrec, 1) * 1e3, 2) for k, v in kern_ms.items()},
+            "kernels_note": "per-kernel averages from a second pass of %d steps with events "
+                            "around each kernel" % nrec,
             "gpu_launches": launches,
             "clocks": clocks,
             "e2e": e2e,

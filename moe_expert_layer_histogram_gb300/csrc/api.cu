@@ -14,12 +14,16 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <string>
 #include <vector>
 
 #include "internal.h"
 #include "moe.h"
 
 using namespace moe;
+
+bool moe::g_pdl_small = true;
+bool moe::g_pdl_gemm = true;
 
 struct moe_layer {
   moe_config cfg;
@@ -31,12 +35,12 @@ struct moe_layer {
   int x_tiles_k = 0, h_tiles_k = 0;  // 128x4 scale tiles per 128-row block
   float clamp = INFINITY;
   std::vector<void*> allocs;
-  int32_t *ids = nullptr, *blockhist = nullptr, *base = nullptr, *pbase = nullptr;
+  int32_t *ids = nullptr, *blockhist = nullptr, *prefix = nullptr;
   int32_t *offsets = nullptr, *pad_off = nullptr, *chunk_off = nullptr, *counts = nullptr;
   int32_t *perm = nullptr, *inv = nullptr;
   float* w = nullptr;
   uint8_t *xq = nullptr, *xsf = nullptr, *hq = nullptr, *hsf = nullptr, *y = nullptr;
-  uint8_t *w13 = nullptr, *w13sf = nullptr, *w2 = nullptr, *w2sf = nullptr;
+  uint8_t *w13t = nullptr, *w2t = nullptr;  // prepared weight tiles
   int* status = nullptr;
   uint8_t *h_in = nullptr, *o_out = nullptr;
   float* l_in = nullptr;
@@ -163,6 +167,12 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
     return MOE_ERR_NO_DEVICE;
   }
   if (!encode_fn()) return MOE_ERR_NO_DEVICE;
+  {
+    const char* v = std::getenv("MOE_DISABLE_PDL");
+    const std::string off = v ? v : "";
+    g_pdl_small = !(off == "1" || off == "small");
+    g_pdl_gemm = !(off == "1" || off == "gemm");
+  }
 
   moe_layer* L = new moe_layer;
   L->cfg = c;
@@ -190,8 +200,7 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   Allocator A(L);
   bool ok = A.get(&L->ids, Rmax * 4) && A.get(&L->w, Rmax * 4) &&
             A.get(&L->blockhist, static_cast<size_t>(L->NBmax) * E * 4) &&
-            A.get(&L->base, static_cast<size_t>(L->NBmax) * E * 4) &&
-            A.get(&L->pbase, static_cast<size_t>(L->NBmax) * E * 4) &&
+            A.get(&L->prefix, static_cast<size_t>(L->NBmax) * E * 4) &&
             A.get(&L->offsets, (E + 1) * 4) && A.get(&L->pad_off, (E + 1) * 4) &&
             A.get(&L->chunk_off, (E + 1) * 4) && A.get(&L->counts, E * 4) &&
             A.get(&L->perm, Rmax * 4) && A.get(&L->inv, Rmax * 4) &&
@@ -200,10 +209,10 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
             A.get(&L->hq, static_cast<size_t>(Rpad) * L->hb) &&
             A.get(&L->hsf, rblocks * L->h_tiles_k * 512) &&
             A.get(&L->y, static_cast<size_t>(Rpad) * H * 2) &&
-            A.get(&L->w13, static_cast<size_t>(E) * 2 * I * L->xb) &&
-            A.get(&L->w13sf, static_cast<size_t>(E) * (2 * I / 128) * L->x_tiles_k * 512) &&
-            A.get(&L->w2, static_cast<size_t>(E) * H * L->hb) &&
-            A.get(&L->w2sf, static_cast<size_t>(E) * (H / 128) * L->h_tiles_k * 512) &&
+            A.get(&L->w13t, static_cast<size_t>(E) * (2 * I / 128) * (L->xb / 128) *
+                                weight_tile_bytes(L->fmt)) &&
+            A.get(&L->w2t, static_cast<size_t>(E) * (H / 128) * (L->hb / 128) *
+                               weight_tile_bytes(L->fmt)) &&
             A.get(&L->status, 16) &&
             A.get(&L->h_in, static_cast<size_t>(L->Tmax) * H * 2) &&
             A.get(&L->l_in, static_cast<size_t>(L->Tmax) * E * 4) &&
@@ -222,9 +231,7 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
     ok = make_map(&L->maps1.a[i], L->xq, L->xb, Rpad, 16u << i) &&
          make_map(&L->maps2.a[i], L->hq, L->hb, Rpad, 16u << i);
   }
-  ok = ok && make_map(&L->maps1.b, L->w13, L->xb, static_cast<uint64_t>(E) * 2 * I, 128) &&
-       make_map(&L->maps2.b, L->w2, L->hb, static_cast<uint64_t>(E) * H, 128) &&
-       cudaDeviceSynchronize() == cudaSuccess;
+  ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     free_all(L);
@@ -243,19 +250,13 @@ moe_status moe_prepare_weights(moe_layer* L, const void* w13, const void* w13_sf
   if (L->fmt == MOE_FMT_NVFP4 && (!w13_gs || !w2_gs)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int E = L->E, H = L->H, I = L->I;
-  cudaError_t e = launch_copy_rows(static_cast<const uint8_t*>(w13), L->w13,
-                                   static_cast<int64_t>(E) * 2 * I, L->xb, 2 * I, I, s);
+  cudaError_t e = launch_tile_weights(L->fmt, static_cast<const uint8_t*>(w13),
+                                      static_cast<const uint8_t*>(w13_sf), w13_gs, L->w13t, E,
+                                      2 * I, L->xb, L->x_tiles_k * 4, I, s);
   if (e == cudaSuccess)
-    e = launch_copy_rows(static_cast<const uint8_t*>(w2), L->w2, static_cast<int64_t>(E) * H,
-                         L->hb, H, 0, s);
-  if (e == cudaSuccess && L->fmt != MOE_FMT_BF16) {
-    const bool nv = L->fmt == MOE_FMT_NVFP4;
-    e = launch_sf_tiles(static_cast<const uint8_t*>(w13_sf), L->w13sf, E, 2 * I,
-                        L->x_tiles_k * 4, nv ? w13_gs : nullptr, I, s);
-    if (e == cudaSuccess)
-      e = launch_sf_tiles(static_cast<const uint8_t*>(w2_sf), L->w2sf, E, H, L->h_tiles_k * 4,
-                          nv ? w2_gs : nullptr, 0, s);
-  }
+    e = launch_tile_weights(L->fmt, static_cast<const uint8_t*>(w2),
+                            static_cast<const uint8_t*>(w2_sf), w2_gs, L->w2t, E, H, L->hb,
+                            L->h_tiles_k * 4, 0, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   L->weights_ready = true;
   return MOE_OK;
@@ -280,15 +281,13 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     if (ev) cudaEventRecord(ev[i], s);
   };
   mark(0);
-  cudaError_t e = launch_route_hist(logits, T, E, K, L->ids, L->w, L->blockhist, s);
+  cudaError_t e = launch_route(logits, T, E, K, L->ids, L->w, L->blockhist, s);
   mark(1);
-  if (e == cudaSuccess)
-    e = launch_scan(L->blockhist, NB, E, L->offsets, L->pad_off, L->chunk_off, L->counts, L->base,
-                    L->pbase, s);
+  if (e == cudaSuccess) e = launch_expert_scan(L->blockhist, NB, E, L->prefix, L->counts, s);
   mark(2);
   if (e == cudaSuccess)
-    e = launch_scatter_quant(L->fmt, L->ids, T, E, K, hidden, H, L->base, L->pbase, L->perm,
-                             L->inv, L->xq, L->xsf, s);
+    e = launch_scatter_quant(L->fmt, L->ids, T, E, K, hidden, H, L->prefix, L->counts, L->offsets,
+                             L->pad_off, L->chunk_off, L->perm, L->inv, L->xq, L->xsf, s);
   mark(3);
   const int64_t chunks = max_chunks(L, T);
   if (e == cudaSuccess) {
@@ -299,11 +298,10 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     a.E = E;
     a.n_tiles = I / 64;
     a.num_kb = L->xb / 128;
-    a.b_rows_per_expert = 2 * I;
     a.sfa = L->xsf;
     a.sfa_tiles_k = L->x_tiles_k;
-    a.sfb = L->w13sf;
-    a.sfb_tiles_k = L->x_tiles_k;
+    a.b_tiles = L->w13t;
+    a.b_tile_bytes = weight_tile_bytes(L->fmt);
     a.out = L->hq;
     a.out_ld = L->hb;
     a.out_sf = L->hsf;
@@ -322,11 +320,10 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     a.E = E;
     a.n_tiles = H / 128;
     a.num_kb = L->hb / 128;
-    a.b_rows_per_expert = H;
     a.sfa = L->hsf;
     a.sfa_tiles_k = L->h_tiles_k;
-    a.sfb = L->w2sf;
-    a.sfb_tiles_k = L->h_tiles_k;
+    a.b_tiles = L->w2t;
+    a.b_tile_bytes = weight_tile_bytes(L->fmt);
     a.out = L->y;
     a.out_ld = static_cast<int64_t>(H) * 2;
     a.out_sf = nullptr;

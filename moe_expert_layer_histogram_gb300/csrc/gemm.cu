@@ -12,9 +12,11 @@
 //
 // Structure: one persistent CTA per SM walks the device-built work list
 // (expert, 128-column weight tile, 128-row token chunk).  Warp 0 (one
-// thread) streams 128-byte K slices of the activation tile and the weight
-// tile with TMA, plus their scale tiles with bulk copies, into a 6-stage
-// shared-memory ring.  Warp 1 (one thread) owns TMEM: it copies the scale
+// thread) streams 128-byte K slices into a 6-stage shared-memory ring: the
+// activation tile by TMA (box height = the chunk's real rows, rounded up to
+// 16/32/64/128) plus its scale tiles, and the weight tile with its scales as
+// one contiguous pre-swizzled bulk copy.  Stage layout: A codes (16 KiB),
+// B codes (16 KiB), B scales, A scales.  Warp 1 (one thread) owns TMEM: it copies the scale
 // tiles into TMEM (tcgen05.cp) and issues 128x128 tcgen05.mma into one of two
 // 128-column fp32 accumulators.  Warps 2-5 drain the other accumulator
 // (tcgen05.ld), run the epilogue and store.  The token tile is the MMA's M
@@ -56,9 +58,13 @@ __host__ __device__ constexpr int stage_bytes() {
   return 2 * kTileBytes + 2 * Fmt<FMT>::kSfTiles * 512;
 }
 
+// Per-expert item tables kept in shared memory: chunk_off[E+1],
+// pad_off[E], counts[E].
+constexpr int kTableInts = 3 * (kMaxExperts + 1);
+
 template <int FMT>
 __host__ __device__ constexpr int smem_bytes() {
-  return 1024 + kGemmStages * stage_bytes<FMT>() + (2 * kGemmStages + 5) * 8 + 16;
+  return 1024 + kGemmStages * stage_bytes<FMT>() + (2 * kGemmStages + 5) * 8 + 16 + kTableInts * 4;
 }
 
 struct Item {
@@ -67,21 +73,28 @@ struct Item {
 
 // Work item -> (expert, weight tile, chunk).  Items are numbered expert-major:
 // expert e owns items [chunk_off[e] * n_tiles, chunk_off[e+1] * n_tiles).
-__device__ __forceinline__ Item map_item(const GemmArgs& a, int item) {
-  int lo = 0, hi = a.E;  // chunk_off[lo]*nt <= item < chunk_off[hi]*nt
+// The tables live in shared memory (loaded once per CTA).
+struct Tables {
+  const int* chunk_off;  // [E+1]
+  const int* pad_off;    // [E]
+  const int* counts;     // [E]
+};
+
+__device__ __forceinline__ Item map_item(const Tables& t, int E, int n_tiles, int item) {
+  int lo = 0, hi = E;  // chunk_off[lo]*nt <= item < chunk_off[hi]*nt
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(a.chunk_off + mid) * a.n_tiles <= item) lo = mid; else hi = mid;
+    if (t.chunk_off[mid] * n_tiles <= item) lo = mid; else hi = mid;
   }
-  const int c0 = __ldg(a.chunk_off + lo);
-  const int nch = __ldg(a.chunk_off + lo + 1) - c0;
-  const int local = item - c0 * a.n_tiles;
+  const int c0 = t.chunk_off[lo];
+  const int nch = t.chunk_off[lo + 1] - c0;
+  const int local = item - c0 * n_tiles;
   const int chunk = local % nch;
   Item it;
   it.e = lo;
   it.n_tile = local / nch;
-  it.prow0 = __ldg(a.pad_off + lo) + chunk * kRowBlock;
-  it.rows = min(kRowBlock, __ldg(a.counts + lo) - chunk * kRowBlock);
+  it.prow0 = t.pad_off[lo] + chunk * kRowBlock;
+  it.rows = min(kRowBlock, t.counts[lo] - chunk * kRowBlock);
   return it;
 }
 
@@ -214,6 +227,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* drained = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_tab = reinterpret_cast<int*>(tmem_holder + 4);
+  const Tables tab{s_tab, s_tab + (args.E + 1), s_tab + (2 * args.E + 1)};
+  pdl_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -233,29 +249,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
+  if (threadIdx.x == 32 * 2)
+    for (int i = 0; i < 4; ++i) prefetch_tmap(&maps.a[i]);
+  // Everything below reads what the previous kernels wrote.
+  pdl_wait();
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_tab[i] = args.chunk_off[i];
+  for (int i = threadIdx.x; i < args.E; i += blockDim.x) {
+    s_tab[args.E + 1 + i] = args.pad_off[i];
+    s_tab[2 * args.E + 1 + i] = args.counts[i];
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const int total = __ldg(args.chunk_off + args.E) * args.n_tiles;
+  const int total = tab.chunk_off[args.E] * args.n_tiles;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      for (int i = 0; i < 4; ++i) prefetch_tmap(&maps.a[i]);
-      prefetch_tmap(&maps.b);
       const uint64_t policy = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const Item it = map_item(args, item);
+        const Item it = map_item(tab, args.E, args.n_tiles, item);
         const int amap = it.rows <= 16 ? 0 : it.rows <= 32 ? 1 : it.rows <= 64 ? 2 : 3;
-        const uint32_t bytes = (16u << amap) * 128u + kTileBytes + 2u * SFT * 512u;
-        const int brow0 = it.e * args.b_rows_per_expert + it.n_tile * 128;
+        const uint32_t bytes = (16u << amap) * 128u + args.b_tile_bytes + SFT * 512u;
         const uint8_t* sfa = args.sfa + static_cast<int64_t>(it.prow0 >> 7) * args.sfa_tiles_k * 512;
-        const uint8_t* sfb = args.sfb + static_cast<int64_t>(brow0 >> 7) * args.sfb_tiles_k * 512;
+        const uint8_t* btile =
+            args.b_tiles + (static_cast<int64_t>(it.e) * args.n_tiles + it.n_tile) * args.num_kb *
+                               args.b_tile_bytes;
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -264,11 +288,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sp = smem + stage * SB;
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sp, &maps.a[amap], &full[stage], kb * 128, it.prow0);
-          tma_load_2d_hint(sp + kTileBytes, &maps.b, &full[stage], kb * 128, brow0, policy);
-          if constexpr (SFT > 0) {
-            bulk_load(sp + 2 * kTileBytes, sfa + kb * SFT * 512, SFT * 512, &full[stage]);
-            bulk_load(sp + 2 * kTileBytes + SFT * 512, sfb + kb * SFT * 512, SFT * 512, &full[stage]);
-          }
+          // weight tile codes + its scale tiles: one contiguous block
+          bulk_load_hint(sp + kTileBytes, btile + static_cast<int64_t>(kb) * args.b_tile_bytes,
+                         args.b_tile_bytes, &full[stage], policy);
+          if constexpr (SFT > 0)
+            bulk_load(sp + 2 * kTileBytes + SFT * 512, sfa + kb * SFT * 512, SFT * 512, &full[stage]);
           ++issued;
           if (++stage == kGemmStages) {
             stage = 0;
@@ -316,16 +340,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if constexpr (FMT == kFmtNVFP4) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              tc_copy_sf(sf_col + j * 8, desc_sf(smem_u32(sp + 2 * kTileBytes + j * 512)));
-              tc_copy_sf(sf_col + j * 8 + 4, desc_sf(smem_u32(sp + 2 * kTileBytes + (4 + j) * 512)));
+              tc_copy_sf(sf_col + j * 8, desc_sf(smem_u32(sp + 2 * kTileBytes + (4 + j) * 512)));
+              tc_copy_sf(sf_col + j * 8 + 4, desc_sf(smem_u32(sp + 2 * kTileBytes + j * 512)));
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
                        sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
           } else if constexpr (FMT == kFmtMXFP8) {
-            tc_copy_sf(sf_col, desc_sf(smem_u32(sp + 2 * kTileBytes)));
-            tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sp + 2 * kTileBytes + 512)));
+            tc_copy_sf(sf_col, desc_sf(smem_u32(sp + 2 * kTileBytes + 512)));
+            tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sp + 2 * kTileBytes)));
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
@@ -354,7 +378,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int local = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++local) {
-      const Item it = map_item(args, item);
+      const Item it = map_item(tab, args.E, args.n_tiles, item);
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(&tfull[buf], use & 1u, abort_flag)) {
@@ -383,8 +407,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 template <int FMT, int EPI>
 cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t s) {
-  moe_gemm_kernel<FMT, EPI><<<grid, kGemmThreads, smem_bytes<FMT>(), s>>>(maps, args);
-  return cudaGetLastError();
+  return launch_pdl(g_pdl_gemm, moe_gemm_kernel<FMT, EPI>, dim3(grid), dim3(kGemmThreads),
+                    smem_bytes<FMT>(), s, maps, args);
 }
 
 template <int FMT>

@@ -12,7 +12,7 @@ constexpr int kFmtBF16 = 0, kFmtMXFP8 = 1, kFmtNVFP4 = 2;
 
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
-constexpr int kTokensPerRouteBlock = 64;  // tokens per routing/scatter block
+constexpr int kTokensPerRouteBlock = 8;   // tokens per routing/scatter block (warp each)
 constexpr int kRowBlock = 128;            // expert segments padded to this
 constexpr int kGemmStages = 6;            // shared-memory pipeline depth
 constexpr int kGemmThreads = 192;         // producer, MMA, 4 epilogue warps
@@ -27,11 +27,10 @@ struct GemmArgs {
   int E;
   int n_tiles;               // output tiles per expert
   int num_kb;                // 128-byte K stages per item
-  int b_rows_per_expert;     // weight rows per expert (2I or H)
   const uint8_t* sfa;        // activation scales, 128x4 tiles
   int sfa_tiles_k;
-  const uint8_t* sfb;        // weight scales, 128x4 tiles
-  int sfb_tiles_k;
+  const uint8_t* b_tiles;    // weight tiles (see weight_tile_bytes), expert-major
+  int b_tile_bytes;
   uint8_t* out;              // GEMM1: GEMM2 input codes; GEMM2: y (bf16)
   int64_t out_ld;            // bytes per output row
   uint8_t* out_sf;           // GEMM1 (MX/NV): GEMM2 input scales
@@ -42,8 +41,49 @@ struct GemmArgs {
 
 struct GemmMaps {
   CUtensorMap a[4];  // activation rows, boxes of 16/32/64/128 rows x 128 B
-  CUtensorMap b;     // weight rows, box 128 rows x 128 B
 };
+
+// Prepared weights are stored as tiles, one per (expert, 128-row block of
+// the weight matrix, 128-byte slice of the reduction dimension), in that
+// order.  A tile is 16 KiB of codes -- 128 rows of 128 bytes, already in the
+// 128-byte-swizzled order the MMA descriptors expect (16-byte chunk c of row
+// r stored at chunk c ^ (r % 8)) -- followed by the slice's block-scale
+// tiles (NVFP4: 4 x 512 bytes, MXFP8: 1 x 512, BF16: none).  One stage of
+// a GEMM fetches one tile with one contiguous bulk copy.
+constexpr int weight_sf_tiles(int fmt) { return fmt == kFmtNVFP4 ? 4 : fmt == kFmtMXFP8 ? 1 : 0; }
+constexpr int weight_tile_bytes(int fmt) { return 128 * 128 + 512 * weight_sf_tiles(fmt); }
+
+// Programmatic dependent launch: every kernel of the forward is launched
+// with programmatic stream serialization, lets its dependents launch as soon
+// as it starts, runs its input-independent prologue and waits for the
+// previous kernel (griddepcontrol.wait) before it touches data that kernel
+// produced or still reads.  It can be switched off for comparison, read at
+// moe_create: MOE_DISABLE_PDL=1 (all kernels), =gemm (the two GEMMs),
+// =small (the others).
+extern bool g_pdl_small, g_pdl_gemm;
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
 
 size_t gemm_smem_bytes(int fmt);
 cudaError_t gemm_prepare(int fmt);  // raise the dynamic shared-memory limit
@@ -51,23 +91,22 @@ cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& 
                         cudaStream_t s);
 
 // Routing, permutation + activation quantisation, combine.
-cudaError_t launch_route_hist(const float* logits, int T, int E, int K, int32_t* ids, float* w,
-                              int32_t* blockhist, cudaStream_t s);
-cudaError_t launch_scan(const int32_t* blockhist, int NB, int E, int32_t* offsets,
-                        int32_t* pad_off, int32_t* chunk_off, int32_t* counts, int32_t* base,
-                        int32_t* pbase, cudaStream_t s);
+cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* w,
+                         int32_t* blockhist, cudaStream_t s);
+cudaError_t launch_expert_scan(const int32_t* blockhist, int NB, int E, int32_t* prefix,
+                               int32_t* counts, cudaStream_t s);
 cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int K,
-                                 const void* hidden, int H, const int32_t* base,
-                                 const int32_t* pbase, int32_t* perm, int32_t* inv, uint8_t* xq,
+                                 const void* hidden, int H, const int32_t* prefix,
+                                 const int32_t* counts, int32_t* offsets, int32_t* pad_off,
+                                 int32_t* chunk_off, int32_t* perm, int32_t* inv, uint8_t* xq,
                                  uint8_t* xsf, cudaStream_t s);
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int K, int H,
                            void* out, cudaStream_t s);
 
 // Weight preparation.
-cudaError_t launch_copy_rows(const uint8_t* src, uint8_t* dst, int64_t rows, int64_t row_bytes,
-                             int N, int interleave_half, cudaStream_t s);
-cudaError_t launch_sf_tiles(const uint8_t* src, uint8_t* dst, int E, int N, int nkg,
-                            const float* gs, int interleave_half, cudaStream_t s);
+cudaError_t launch_tile_weights(int fmt, const uint8_t* codes, const uint8_t* sf, const float* gs,
+                                uint8_t* tiles, int E, int N, int row_bytes, int nkg,
+                                int interleave_half, cudaStream_t s);
 
 // Inspection.
 cudaError_t launch_debug_act(int fmt, const int32_t* inv, int T, int K, int H, const uint8_t* xq,

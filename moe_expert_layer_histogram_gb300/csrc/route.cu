@@ -7,8 +7,8 @@
 // steps of the fused layer, which the b12x integration runs together with
 // both expert GEMMs in one call (PR #40082 report, sec. 实现拆解 item 1).  The
 // permutation is the single-GPU form of token dispatch: slots (t, k) are grouped by
-// expert with a stable counting sort (histogram per block of 64 tokens, an
-// exclusive scan over (expert, block), a scatter), and each expert's segment
+// expert with a stable counting sort (histogram per block of 8 tokens, an
+// exclusive scan over the blocks per expert, a scatter), and each expert's segment
 // is padded to a multiple of 128 rows so every 128-row GEMM tile and its
 // scale tiles start on a tile boundary.
 #include <cuda_bf16.h>
@@ -26,22 +26,24 @@ namespace {
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // ---------------------------------------------------------------- routing
-// One warp per token.  Lane l holds logits l, l+32, ...; K rounds of a warp
-// arg-max in the total order (value descending, index ascending), then the
-// softmax of the K selected values.  Also counts, per block of 64 tokens,
-// how many slots go to each expert.
+// One warp per token, 8 tokens per block.  Lane l holds logits l, l+32, ...;
+// K rounds of a warp arg-max in the total order (value descending, index
+// ascending), then the softmax of the K selected values.  Block b also counts
+// how many of its slots go to each expert (blockhist[b][e]).
 template <int MAXJ>
-__global__ void __launch_bounds__(256) route_hist_kernel(const float* __restrict__ logits, int T,
-                                                         int E, int K, int32_t* __restrict__ ids,
-                                                         float* __restrict__ w,
-                                                         int32_t* __restrict__ blockhist) {
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E,
+                                                    int K, int32_t* __restrict__ ids,
+                                                    float* __restrict__ w,
+                                                    int32_t* __restrict__ blockhist) {
+  pdl_launch_dependents();
   __shared__ int hist[kMaxExperts];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = warp; i < kTokensPerRouteBlock; i += 8) {
-    const int t = blockIdx.x * kTokensPerRouteBlock + i;
-    if (t >= T) break;
+  const int t = blockIdx.x * kTokensPerRouteBlock + warp;
+  float my_v = 0.0f, ex = 0.0f, sum = 1.0f;
+  int my_i = 0;
+  if (t < T) {
     const float* l = logits + static_cast<int64_t>(t) * E;
     float v[MAXJ];
     uint32_t avail = 0;
@@ -54,8 +56,6 @@ __global__ void __launch_bounds__(256) route_hist_kernel(const float* __restrict
         avail |= 1u << j;
       }
     }
-    float my_v = 0.0f;
-    int my_i = 0;
     for (int k = 0; k < K; ++k) {
       float bv = -FLT_MAX;
       int bi = INT_MAX;
@@ -82,15 +82,17 @@ __global__ void __launch_bounds__(256) route_hist_kernel(const float* __restrict
       }
     }
     const float m = __shfl_sync(kFull, my_v, 0);
-    const float ex = lane < K ? expf(my_v - m) : 0.0f;
-    float sum = ex;
+    ex = lane < K ? expf(my_v - m) : 0.0f;
+    sum = ex;
 #pragma unroll
     for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-    if (lane < K) {
-      ids[static_cast<int64_t>(t) * K + lane] = my_i;
-      w[static_cast<int64_t>(t) * K + lane] = ex / sum;
-      atomicAdd(&hist[my_i], 1);
-    }
+  }
+  // the previous forward's last kernels may still read ids / w / blockhist
+  pdl_wait();
+  if (t < T && lane < K) {
+    ids[static_cast<int64_t>(t) * K + lane] = my_i;
+    w[static_cast<int64_t>(t) * K + lane] = ex / sum;
+    atomicAdd(&hist[my_i], 1);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -98,88 +100,128 @@ __global__ void __launch_bounds__(256) route_hist_kernel(const float* __restrict
 }
 
 // ---------------------------------------------------------------- scan
-// One block, thread e = expert.  Per-expert counts, exclusive scans of the
-// counts, of the 128-padded counts and of the 128-row chunk counts, and the
-// first (unpadded / padded) row of every (routing block, expert) pair.
-__global__ void __launch_bounds__(kMaxExperts) scan_kernel(
-    const int32_t* __restrict__ blockhist, int NB, int E, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ pad_off, int32_t* __restrict__ chunk_off, int32_t* __restrict__ counts,
-    int32_t* __restrict__ base, int32_t* __restrict__ pbase) {
-  __shared__ int wsum[3][kMaxExperts / 32];
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  int c = 0;
-  if (e < E) {
-#pragma unroll 8
-    for (int b = 0; b < NB; ++b) c += blockhist[static_cast<int64_t>(b) * E + e];
-  }
-  int v[3] = {c, (c + kRowBlock - 1) / kRowBlock * kRowBlock, (c + kRowBlock - 1) / kRowBlock};
-  int inc[3] = {v[0], v[1], v[2]};
+// One warp per expert: exclusive scan of the expert's per-block counts over
+// the routing blocks (prefix[b][e] = slots of expert e in blocks < b) and its
+// total count.
+__global__ void __launch_bounds__(256) expert_scan_kernel(const int32_t* __restrict__ blockhist,
+                                                          int NB, int E,
+                                                          int32_t* __restrict__ prefix,
+                                                          int32_t* __restrict__ counts) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  if (e >= E) return;
+  const int per = (NB + 31) / 32;
+  const int b0 = lane * per, b1 = min(NB, b0 + per);
+  int sum = 0;
+  for (int b = b0; b < b1; ++b) sum += blockhist[static_cast<int64_t>(b) * E + e];
+  int inc = sum;
 #pragma unroll
-  for (int q = 0; q < 3; ++q) {
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(kFull, inc[q], off);
-      if (lane >= off) inc[q] += o;
-    }
-    if (lane == 31) wsum[q][warp] = inc[q];
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(kFull, inc, off);
+    if (lane >= off) inc += o;
   }
+  int run = inc - sum;
+  for (int b = b0; b < b1; ++b) {
+    const int64_t i = static_cast<int64_t>(b) * E + e;
+    const int c = blockhist[i];
+    prefix[i] = run;
+    run += c;
+  }
+  if (lane == 31) counts[e] = inc;
+}
+
+// Block-wide exclusive scan of one value per thread (256 threads, each
+// thread's value covering two experts).
+__device__ __forceinline__ int block_scan_pair(int v, int* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(kFull, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) wsum[warp] = inc;
   __syncthreads();
-  int ex[3];
-#pragma unroll
-  for (int q = 0; q < 3; ++q) {
-    int add = 0;
-    for (int w2 = 0; w2 < warp; ++w2) add += wsum[q][w2];
-    ex[q] = inc[q] - v[q] + add;
-  }
-  if (e < E) {
-    offsets[e] = ex[0];
-    pad_off[e] = ex[1];
-    chunk_off[e] = ex[2];
-    counts[e] = c;
-    if (e == E - 1) {
-      offsets[E] = ex[0] + v[0];
-      pad_off[E] = ex[1] + v[1];
-      chunk_off[E] = ex[2] + v[2];
-    }
-    int run = 0;
-    for (int b = 0; b < NB; ++b) {
-      const int64_t i = static_cast<int64_t>(b) * E + e;
-      base[i] = ex[0] + run;
-      pbase[i] = ex[1] + run;
-      run += blockhist[i];
-    }
-  }
+  int add = 0;
+  for (int w2 = 0; w2 < warp; ++w2) add += wsum[w2];
+  __syncthreads();
+  return inc - v + add;
 }
 
 // ---------------------------------------------------------------- scatter
-// Block b handles the 64 tokens of routing block b.  Warp 0 assigns, in slot
-// order, each slot its rank among the block's slots of the same expert
-// (stable), giving perm[row] = slot and the padded row of each slot.  Then
-// all warps write every token's GEMM1 input into its K padded rows:
-// BF16 copied, MXFP8 / NVFP4 quantised per block (one block per lane).
+// Block b handles the 8 tokens of routing block b.
+//  1. Exclusive scans of the per-expert counts, 128-padded counts and 128-row
+//     chunk counts (every block computes them; block 0 stores them for the
+//     GEMMs).
+//  2. Warp 0 gives each of the block's slots, in slot order, the next row of
+//     its expert after the rows of earlier blocks (stable): perm[row] = slot,
+//     inv[slot] = padded row.
+//  3. Warp w writes token 8b+w's GEMM1 input into its K padded rows: BF16
+//     copied, MXFP8 / NVFP4 quantised per block (one block per lane).
 template <int FMT>
 __global__ void __launch_bounds__(256) scatter_quant_kernel(
     const int32_t* __restrict__ ids, int T, int E, int K, const __nv_bfloat16* __restrict__ hidden,
-    int H, const int32_t* __restrict__ base, const int32_t* __restrict__ pbase,
+    int H, const int32_t* __restrict__ prefix, const int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ pad_off, int32_t* __restrict__ chunk_off,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv, uint8_t* __restrict__ xq,
     uint8_t* __restrict__ xsf) {
-  __shared__ int cnt[kMaxExperts];
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts], cnt[kMaxExperts];
   __shared__ int s_prow[kTokensPerRouteBlock * kMaxTopK];
+  __shared__ int wsum[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok0 = blockIdx.x * kTokensPerRouteBlock;
   const int ntok = min(kTokensPerRouteBlock, T - tok0);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+
+  // 1. offsets
+  const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
+  const int c0 = e0 < E ? counts[e0] : 0, c1 = e1 < E ? counts[e1] : 0;
+  const int p0 = (c0 + kRowBlock - 1) / kRowBlock, p1 = (c1 + kRowBlock - 1) / kRowBlock;
+  const int xo = block_scan_pair(c0 + c1, wsum);
+  const int xp = block_scan_pair((p0 + p1) * kRowBlock, wsum);
+  const int xc = block_scan_pair(p0 + p1, wsum);
+  if (e0 < E) {
+    s_off[e0] = xo;
+    s_poff[e0] = xp;
+    cnt[e0] = 0;
+  }
+  if (e1 < E) {
+    s_off[e1] = xo + c0;
+    s_poff[e1] = xp + p0 * kRowBlock;
+    cnt[e1] = 0;
+  }
+  if (blockIdx.x == 0) {
+    if (e0 < E) {
+      offsets[e0] = xo;
+      pad_off[e0] = xp;
+      chunk_off[e0] = xc;
+    }
+    if (e1 < E) {
+      offsets[e1] = xo + c0;
+      pad_off[e1] = xp + p0 * kRowBlock;
+      chunk_off[e1] = xc + p0;
+    }
+    if (e0 == E - 1 || e1 == E - 1) {
+      offsets[E] = xo + c0 + c1;
+      pad_off[E] = xp + (p0 + p1) * kRowBlock;
+      chunk_off[E] = xc + p0 + p1;
+    }
+  }
   __syncthreads();
+
+  // 2. stable ranks
   if (warp == 0) {
     for (int i = 0; i < ntok; ++i) {
       const int64_t s = static_cast<int64_t>(tok0 + i) * K + lane;
       if (lane < K) {
         const int e = ids[s];
-        const int r = cnt[e];
-        cnt[e] = r + 1;  // the K experts of one token are distinct
-        const int64_t bi = static_cast<int64_t>(blockIdx.x) * E + e;
-        perm[base[bi] + r] = static_cast<int32_t>(s);
-        const int prow = pbase[bi] + r;
+        const int r = cnt[e] + prefix[static_cast<int64_t>(blockIdx.x) * E + e];
+        cnt[e] += 1;  // the K experts of one token are distinct
+        perm[s_off[e] + r] = static_cast<int32_t>(s);
+        const int prow = s_poff[e] + r;
         inv[s] = prow;
         s_prow[i * K + lane] = prow;
       }
@@ -188,67 +230,67 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
   }
   __syncthreads();
 
-  for (int i = warp; i < ntok; i += 8) {
-    const __nv_bfloat16* x = hidden + static_cast<int64_t>(tok0 + i) * H;
-    const int* prows = s_prow + i * K;
-    if constexpr (FMT == kFmtBF16) {
-      const uint4* src = reinterpret_cast<const uint4*>(x);
-      for (int c = lane; c < H / 8; c += 32) {
-        const uint4 val = src[c];
-        for (int k = 0; k < K; ++k)
-          reinterpret_cast<uint4*>(xq + static_cast<int64_t>(prows[k]) * H * 2)[c] = val;
-      }
-    } else if constexpr (FMT == kFmtNVFP4) {
-      const int tiles_k = H / 64;
-      for (int blk = lane; blk < H / 16; blk += 32) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + blk * 16);
-        float f[16];
+  // 3. GEMM1 input rows
+  if (warp >= ntok) return;
+  const __nv_bfloat16* x = hidden + static_cast<int64_t>(tok0 + warp) * H;
+  const int* prows = s_prow + warp * K;
+  if constexpr (FMT == kFmtBF16) {
+    const uint4* src = reinterpret_cast<const uint4*>(x);
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 val = src[c];
+      for (int k = 0; k < K; ++k)
+        reinterpret_cast<uint4*>(xq + static_cast<int64_t>(prows[k]) * H * 2)[c] = val;
+    }
+  } else if constexpr (FMT == kFmtNVFP4) {
+    const int tiles_k = H / 64;
+    for (int blk = lane; blk < H / 16; blk += 32) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + blk * 16);
+      float f[16];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint4 u = src[h];
-          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+      for (int h = 0; h < 2; ++h) {
+        const uint4 u = src[h];
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
-            f[8 * h + 2 * q] = p.x;
-            f[8 * h + 2 * q + 1] = p.y;
-          }
-        }
-        uint32_t codes[2];
-        uint8_t sf;
-        quant_nvfp4_16(f, codes, sf);
-        for (int k = 0; k < K; ++k) {
-          const int64_t prow = prows[k];
-          *reinterpret_cast<uint2*>(xq + prow * (H / 2) + blk * 8) = make_uint2(codes[0], codes[1]);
-          xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
+        for (int q = 0; q < 4; ++q) {
+          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+          f[8 * h + 2 * q] = p.x;
+          f[8 * h + 2 * q + 1] = p.y;
         }
       }
-    } else {
-      const int tiles_k = H / 128;
-      for (int blk = lane; blk < H / 32; blk += 32) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + blk * 32);
-        float f[32];
+      uint32_t codes[2];
+      uint8_t sf;
+      quant_nvfp4_16(f, codes, sf);
+      for (int k = 0; k < K; ++k) {
+        const int64_t prow = prows[k];
+        *reinterpret_cast<uint2*>(xq + prow * (H / 2) + blk * 8) = make_uint2(codes[0], codes[1]);
+        xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
+      }
+    }
+  } else {
+    const int tiles_k = H / 128;
+    for (int blk = lane; blk < H / 32; blk += 32) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + blk * 32);
+      float f[32];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const uint4 u = src[h];
-          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+      for (int h = 0; h < 4; ++h) {
+        const uint4 u = src[h];
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
-            f[8 * h + 2 * q] = p.x;
-            f[8 * h + 2 * q + 1] = p.y;
-          }
+        for (int q = 0; q < 4; ++q) {
+          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+          f[8 * h + 2 * q] = p.x;
+          f[8 * h + 2 * q + 1] = p.y;
         }
-        uint32_t codes[8];
-        uint8_t sf;
-        quant_mxfp8_32(f, codes, sf);
-        for (int k = 0; k < K; ++k) {
-          const int64_t prow = prows[k];
-          uint4* dst = reinterpret_cast<uint4*>(xq + prow * H + blk * 32);
-          dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-          dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-          xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
-        }
+      }
+      uint32_t codes[8];
+      uint8_t sf;
+      quant_mxfp8_32(f, codes, sf);
+      for (int k = 0; k < K; ++k) {
+        const int64_t prow = prows[k];
+        uint4* dst = reinterpret_cast<uint4*>(xq + prow * H + blk * 32);
+        dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
       }
     }
   }
@@ -256,12 +298,14 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
 
 // ---------------------------------------------------------------- combine
 // out[t] = bf16( sum_k w[t,k] * y[row(t,k)] ), fp32 accumulation in k order.
-// One block per token; each thread owns 8 consecutive columns (16-byte
-// loads and stores, coalesced along H).
+// Grid (T, H/1024): each thread owns 8 consecutive columns (16-byte loads and
+// stores, coalesced along H).
 __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ y,
                                                       const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int K, int H,
                                                       __nv_bfloat16* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ int64_t s_row[kMaxTopK];
   __shared__ float s_w[kMaxTopK];
   const int t = blockIdx.x;
@@ -270,29 +314,29 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
     s_w[threadIdx.x] = w[static_cast<int64_t>(t) * K + threadIdx.x];
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
-    float acc[8];
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;
+  if (c >= H / 8) return;
+  float acc[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int k = 0; k < K; ++k) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(y + s_row[k] * H) + c);
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-      const float wk = s_w[k];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
-        acc[2 * q] = fmaf(wk, p.x, acc[2 * q]);
-        acc[2 * q + 1] = fmaf(wk, p.y, acc[2 * q + 1]);
-      }
-    }
-    uint32_t o[4];
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  for (int k = 0; k < K; ++k) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(y + s_row[k] * H) + c);
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+    const float wk = s_w[k];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-      o[q] = *reinterpret_cast<const uint32_t*>(&b);
+      const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+      acc[2 * q] = fmaf(wk, p.x, acc[2 * q]);
+      acc[2 * q + 1] = fmaf(wk, p.y, acc[2 * q + 1]);
     }
-    reinterpret_cast<uint4*>(out + static_cast<int64_t>(t) * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+    o[q] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  reinterpret_cast<uint4*>(out + static_cast<int64_t>(t) * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ---------------------------------------------------------------- inspection
@@ -349,49 +393,40 @@ __global__ void debug_rows_kernel(int fmt, const int32_t* __restrict__ offsets,
 
 }  // namespace
 
-cudaError_t launch_route_hist(const float* logits, int T, int E, int K, int32_t* ids, float* w,
-                              int32_t* blockhist, cudaStream_t s) {
+cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* w,
+                         int32_t* blockhist, cudaStream_t s) {
   const int nb = (T + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
-  if (E <= 128)
-    route_hist_kernel<4><<<nb, 256, 0, s>>>(logits, T, E, K, ids, w, blockhist);
-  else if (E <= 256)
-    route_hist_kernel<8><<<nb, 256, 0, s>>>(logits, T, E, K, ids, w, blockhist);
-  else
-    route_hist_kernel<16><<<nb, 256, 0, s>>>(logits, T, E, K, ids, w, blockhist);
-  return cudaGetLastError();
+  auto k = E <= 128 ? route_kernel<4> : E <= 256 ? route_kernel<8> : route_kernel<16>;
+  return launch_pdl(g_pdl_small, k, dim3(nb), dim3(256), 0, s, logits, T, E, K, ids, w,
+                    blockhist);
 }
 
-cudaError_t launch_scan(const int32_t* blockhist, int NB, int E, int32_t* offsets,
-                        int32_t* pad_off, int32_t* chunk_off, int32_t* counts, int32_t* base,
-                        int32_t* pbase, cudaStream_t s) {
-  scan_kernel<<<1, kMaxExperts, 0, s>>>(blockhist, NB, E, offsets, pad_off, chunk_off, counts,
-                                        base, pbase);
-  return cudaGetLastError();
+cudaError_t launch_expert_scan(const int32_t* blockhist, int NB, int E, int32_t* prefix,
+                               int32_t* counts, cudaStream_t s) {
+  return launch_pdl(g_pdl_small, expert_scan_kernel, dim3((E + 7) / 8), dim3(256), 0, s,
+                    blockhist, NB, E, prefix, counts);
 }
 
 cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int K,
-                                 const void* hidden, int H, const int32_t* base,
-                                 const int32_t* pbase, int32_t* perm, int32_t* inv, uint8_t* xq,
+                                 const void* hidden, int H, const int32_t* prefix,
+                                 const int32_t* counts, int32_t* offsets, int32_t* pad_off,
+                                 int32_t* chunk_off, int32_t* perm, int32_t* inv, uint8_t* xq,
                                  uint8_t* xsf, cudaStream_t s) {
   const int nb = (T + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
   const auto* hb = static_cast<const __nv_bfloat16*>(hidden);
-  if (fmt == kFmtBF16)
-    scatter_quant_kernel<kFmtBF16><<<nb, 256, 0, s>>>(ids, T, E, K, hb, H, base, pbase, perm, inv,
-                                                      xq, xsf);
-  else if (fmt == kFmtMXFP8)
-    scatter_quant_kernel<kFmtMXFP8><<<nb, 256, 0, s>>>(ids, T, E, K, hb, H, base, pbase, perm,
-                                                       inv, xq, xsf);
-  else
-    scatter_quant_kernel<kFmtNVFP4><<<nb, 256, 0, s>>>(ids, T, E, K, hb, H, base, pbase, perm,
-                                                       inv, xq, xsf);
-  return cudaGetLastError();
+  auto k = fmt == kFmtBF16 ? scatter_quant_kernel<kFmtBF16>
+           : fmt == kFmtMXFP8 ? scatter_quant_kernel<kFmtMXFP8>
+                              : scatter_quant_kernel<kFmtNVFP4>;
+  return launch_pdl(g_pdl_small, k, dim3(nb), dim3(256), 0, s, ids, T, E, K, hb, H, prefix,
+                    counts, offsets, pad_off, chunk_off, perm, inv, xq, xsf);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int K, int H,
                            void* out, cudaStream_t s) {
-  combine_kernel<<<T, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(y), inv, w, K, H,
-                                   static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  const dim3 grid(T, (H / 8 + 127) / 128);
+  return launch_pdl(g_pdl_small, combine_kernel, grid, dim3(128), 0, s,
+                    static_cast<const __nv_bfloat16*>(y), inv, w, K, H,
+                    static_cast<__nv_bfloat16*>(out));
 }
 
 cudaError_t launch_debug_act(int fmt, const int32_t* inv, int T, int K, int H, const uint8_t* xq,
