@@ -309,7 +309,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     a.clamp = L->clamp;
     a.status = L->status;
     const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
-    e = launch_gemm(L->fmt, 1, L->maps1, a, grid, s);
+    e = launch_gemm(L->fmt, 1, L->maps1, a, grid, T, s);
   }
   mark(4);
   if (e == cudaSuccess) {
@@ -331,7 +331,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     a.clamp = INFINITY;
     a.status = L->status;
     const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
-    e = launch_gemm(L->fmt, 2, L->maps2, a, grid, s);
+    e = launch_gemm(L->fmt, 2, L->maps2, a, grid, T, s);
   }
   mark(5);
   if (e == cudaSuccess) e = launch_combine(L->y, L->inv, L->w, T, K, H, out, s);

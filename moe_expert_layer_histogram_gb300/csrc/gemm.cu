@@ -12,11 +12,13 @@
 //
 // Structure: one persistent CTA per SM walks the device-built work list
 // (expert, 128-column weight tile, 128-row token chunk).  Warp 0 (one
-// thread) streams 128-byte K slices into a 6-stage shared-memory ring: the
+// thread) streams 128-byte K slices into a shared-memory ring (6-8 stages): the
 // activation tile by TMA (box height = the chunk's real rows, rounded up to
 // 16/32/64/128) plus its scale tiles, and the weight tile with its scales as
-// one contiguous pre-swizzled bulk copy.  Stage layout: A codes (16 KiB),
-// B codes (16 KiB), B scales, A scales.  Warp 1 (one thread) owns TMEM: it copies the scale
+// one contiguous pre-swizzled bulk copy.  Stage layout: A codes (MROWS x
+// 128 bytes), B codes (16 KiB), B scales, A scales.  The MMA always reads 128
+// A rows; rows past the region belong to the B tile and only feed
+// accumulator rows that are never stored.  Warp 1 (one thread) owns TMEM: it copies the scale
 // tiles into TMEM (tcgen05.cp) and issues 128x128 tcgen05.mma into one of two
 // 128-column fp32 accumulators.  Warps 2-5 drain the other accumulator
 // (tcgen05.ld), run the epilogue and store.  The token tile is the MMA's M
@@ -53,18 +55,33 @@ struct Fmt<kFmtNVFP4> {
   static constexpr int kSfTiles = 4;  // 256 K elements = 16 x 16-blocks
 };
 
-template <int FMT>
+// A stage holds the activation tile (MROWS rows x 128 bytes), the weight
+// tile (128 rows x 128 bytes) with its scale tiles right after it, and the
+// activation scale tiles.  MROWS is an upper bound on the real rows of any
+// chunk of the launch (rows per expert never exceed T), so decode launches
+// keep a short activation region and fit more stages.
+template <int FMT, int MROWS>
 __host__ __device__ constexpr int stage_bytes() {
-  return 2 * kTileBytes + 2 * Fmt<FMT>::kSfTiles * 512;
+  return MROWS * 128 + kTileBytes + 2 * Fmt<FMT>::kSfTiles * 512;
 }
 
 // Per-expert item tables kept in shared memory: chunk_off[E+1],
 // pad_off[E], counts[E].
 constexpr int kTableInts = 3 * (kMaxExperts + 1);
+constexpr int kSmemLimit = 232448;  // opt-in maximum per block
+constexpr int kMaxStages = 8;       // TMEM holds 8 stages of scale columns
 
-template <int FMT>
+template <int FMT, int MROWS>
+__host__ __device__ constexpr int num_stages() {
+  return (kSmemLimit - 1024 - kTableInts * 4 - 256) / stage_bytes<FMT, MROWS>() > kMaxStages
+             ? kMaxStages
+             : (kSmemLimit - 1024 - kTableInts * 4 - 256) / stage_bytes<FMT, MROWS>();
+}
+
+template <int FMT, int MROWS>
 __host__ __device__ constexpr int smem_bytes() {
-  return 1024 + kGemmStages * stage_bytes<FMT>() + (2 * kGemmStages + 5) * 8 + 16 + kTableInts * 4;
+  return 1024 + num_stages<FMT, MROWS>() * stage_bytes<FMT, MROWS>() +
+         (2 * num_stages<FMT, MROWS>() + 5) * 8 + 16 + kTableInts * 4;
 }
 
 struct Item {
@@ -213,16 +230,18 @@ __device__ __forceinline__ void epilogue_gemm2(uint32_t taddr, bool store, int64
 }
 
 // ---------------------------------------------------------------- kernel
-template <int FMT, int EPI>
+template <int FMT, int EPI, int MROWS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   constexpr int SFT = Fmt<FMT>::kSfTiles;
-  constexpr int SB = stage_bytes<FMT>();
+  constexpr int SB = stage_bytes<FMT, MROWS>();
+  constexpr int kStages = num_stages<FMT, MROWS>();
+  constexpr int A_BYTES = MROWS * 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGemmStages * SB);
-  uint64_t* empty = full + kGemmStages;
-  uint64_t* tfull = empty + kGemmStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * SB);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drained = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 1);
@@ -233,7 +252,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kGemmStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -275,6 +294,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const Item it = map_item(tab, args.E, args.n_tiles, item);
         const int amap = it.rows <= 16 ? 0 : it.rows <= 32 ? 1 : it.rows <= 64 ? 2 : 3;
+        if ((16 << amap) > MROWS) {   // the host bounded the rows per chunk by MROWS
+          ok = false;
+          break;
+        }
         const uint32_t bytes = (16u << amap) * 128u + args.b_tile_bytes + SFT * 512u;
         const uint8_t* sfa = args.sfa + static_cast<int64_t>(it.prow0 >> 7) * args.sfa_tiles_k * 512;
         const uint8_t* btile =
@@ -289,12 +312,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sp, &maps.a[amap], &full[stage], kb * 128, it.prow0);
           // weight tile codes + its scale tiles: one contiguous block
-          bulk_load_hint(sp + kTileBytes, btile + static_cast<int64_t>(kb) * args.b_tile_bytes,
+          bulk_load_hint(sp + A_BYTES, btile + static_cast<int64_t>(kb) * args.b_tile_bytes,
                          args.b_tile_bytes, &full[stage], policy);
           if constexpr (SFT > 0)
-            bulk_load(sp + 2 * kTileBytes + SFT * 512, sfa + kb * SFT * 512, SFT * 512, &full[stage]);
+            bulk_load(sp + A_BYTES + kTileBytes + SFT * 512, sfa + kb * SFT * 512, SFT * 512,
+                      &full[stage]);
           ++issued;
-          if (++stage == kGemmStages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -302,9 +326,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // Before leaving, make sure no copy this thread issued is still in
       // flight (they all completed already unless the block gave up).
-      for (int back = 1; back <= kGemmStages && back <= issued; ++back) {
+      for (int back = 1; back <= kStages && back <= issued; ++back) {
         const int idx = issued - back;
-        mbar_wait(&full[idx % kGemmStages], static_cast<uint32_t>((idx / kGemmStages) & 1), nullptr);
+        mbar_wait(&full[idx % kStages], static_cast<uint32_t>((idx / kStages) & 1), nullptr);
       }
       if (!ok) report_status(args.status, kStatusTimeout);
     }
@@ -335,21 +359,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           uint8_t* sp = smem + stage * SB;
-          const uint32_t a_addr = smem_u32(sp), b_addr = smem_u32(sp + kTileBytes);
+          const uint32_t a_addr = smem_u32(sp), b_addr = smem_u32(sp + A_BYTES);
+          uint8_t* sf = sp + A_BYTES + kTileBytes;  // weight scales, then activation scales
           const uint32_t sf_col = tmem + kSfColBase + stage * kSfColsPerStage;
           if constexpr (FMT == kFmtNVFP4) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              tc_copy_sf(sf_col + j * 8, desc_sf(smem_u32(sp + 2 * kTileBytes + (4 + j) * 512)));
-              tc_copy_sf(sf_col + j * 8 + 4, desc_sf(smem_u32(sp + 2 * kTileBytes + j * 512)));
+              tc_copy_sf(sf_col + j * 8, desc_sf(smem_u32(sf + (4 + j) * 512)));
+              tc_copy_sf(sf_col + j * 8 + 4, desc_sf(smem_u32(sf + j * 512)));
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
                        sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
           } else if constexpr (FMT == kFmtMXFP8) {
-            tc_copy_sf(sf_col, desc_sf(smem_u32(sp + 2 * kTileBytes + 512)));
-            tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sp + 2 * kTileBytes)));
+            tc_copy_sf(sf_col, desc_sf(smem_u32(sf + 512)));
+            tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf)));
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
@@ -361,7 +386,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                        (kb | j) != 0);
           }
           tc_commit(&empty[stage]);
-          if (++stage == kGemmStages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -405,28 +430,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int FMT, int EPI>
+template <int FMT, int EPI, int MROWS>
 cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t s) {
-  return launch_pdl(g_pdl_gemm, moe_gemm_kernel<FMT, EPI>, dim3(grid), dim3(kGemmThreads),
-                    smem_bytes<FMT>(), s, maps, args);
+  return launch_pdl(g_pdl_gemm, moe_gemm_kernel<FMT, EPI, MROWS>, dim3(grid),
+                    dim3(kGemmThreads), smem_bytes<FMT, MROWS>(), s, maps, args);
+}
+
+template <int FMT, int MROWS>
+cudaError_t prepare_m() {
+  cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<FMT, 1, MROWS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes<FMT, MROWS>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(moe_gemm_kernel<FMT, 2, MROWS>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<FMT, MROWS>());
 }
 
 template <int FMT>
 cudaError_t prepare_one() {
-  cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<FMT, 1>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<FMT>());
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(moe_gemm_kernel<FMT, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem_bytes<FMT>());
+  cudaError_t e = prepare_m<FMT, 32>();
+  if (e == cudaSuccess) e = prepare_m<FMT, 64>();
+  if (e == cudaSuccess) e = prepare_m<FMT, 128>();
+  return e;
+}
+
+template <int FMT, int EPI>
+cudaError_t launch_fmt(const GemmMaps& maps, const GemmArgs& args, int grid, int mrows,
+                       cudaStream_t s) {
+  if (mrows <= 32) return launch_one<FMT, EPI, 32>(maps, args, grid, s);
+  if (mrows <= 64) return launch_one<FMT, EPI, 64>(maps, args, grid, s);
+  return launch_one<FMT, EPI, 128>(maps, args, grid, s);
 }
 
 }  // namespace
-
-size_t gemm_smem_bytes(int fmt) {
-  return fmt == kFmtBF16 ? smem_bytes<kFmtBF16>()
-         : fmt == kFmtMXFP8 ? smem_bytes<kFmtMXFP8>()
-                            : smem_bytes<kFmtNVFP4>();
-}
 
 cudaError_t gemm_prepare(int fmt) {
   return fmt == kFmtBF16 ? prepare_one<kFmtBF16>()
@@ -435,15 +471,15 @@ cudaError_t gemm_prepare(int fmt) {
 }
 
 cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& args, int grid,
-                        cudaStream_t s) {
+                        int max_rows, cudaStream_t s) {
   if (fmt == kFmtBF16)
-    return epi == 1 ? launch_one<kFmtBF16, 1>(maps, args, grid, s)
-                    : launch_one<kFmtBF16, 2>(maps, args, grid, s);
+    return epi == 1 ? launch_fmt<kFmtBF16, 1>(maps, args, grid, max_rows, s)
+                    : launch_fmt<kFmtBF16, 2>(maps, args, grid, max_rows, s);
   if (fmt == kFmtMXFP8)
-    return epi == 1 ? launch_one<kFmtMXFP8, 1>(maps, args, grid, s)
-                    : launch_one<kFmtMXFP8, 2>(maps, args, grid, s);
-  return epi == 1 ? launch_one<kFmtNVFP4, 1>(maps, args, grid, s)
-                  : launch_one<kFmtNVFP4, 2>(maps, args, grid, s);
+    return epi == 1 ? launch_fmt<kFmtMXFP8, 1>(maps, args, grid, max_rows, s)
+                    : launch_fmt<kFmtMXFP8, 2>(maps, args, grid, max_rows, s);
+  return epi == 1 ? launch_fmt<kFmtNVFP4, 1>(maps, args, grid, max_rows, s)
+                  : launch_fmt<kFmtNVFP4, 2>(maps, args, grid, max_rows, s);
 }
 
 }  // namespace moe

@@ -14,7 +14,6 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 constexpr int kTokensPerRouteBlock = 8;   // tokens per routing/scatter block (warp each)
 constexpr int kRowBlock = 128;            // expert segments padded to this
-constexpr int kGemmStages = 6;            // shared-memory pipeline depth
 constexpr int kGemmThreads = 192;         // producer, MMA, 4 epilogue warps
 
 // Per-launch arguments of the grouped GEMMs.  Work items are (expert,
@@ -85,10 +84,11 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 #endif
 
-size_t gemm_smem_bytes(int fmt);
 cudaError_t gemm_prepare(int fmt);  // raise the dynamic shared-memory limit
+// max_rows: upper bound on the rows of any expert in this launch (<= T);
+// selects the activation-tile height of the shared-memory stages.
 cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& args, int grid,
-                        cudaStream_t s);
+                        int max_rows, cudaStream_t s);
 
 // Routing, permutation + activation quantisation, combine.
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* w,
