@@ -115,6 +115,14 @@ __device__ __forceinline__ Item map_item(const Tables& t, int E, int n_tiles, in
   return it;
 }
 
+// Accumulator rows past the chunk's real rows come from stale shared memory
+// and may hold NaNs or denormals, which would send the division and exp
+// below down their slow paths; their results are never stored, so those
+// lanes work on zeros instead.
+__device__ __forceinline__ float lane_value(uint32_t bits, bool valid) {
+  return valid ? __uint_as_float(bits) : 0.0f;
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u, float L) {
   g = fminf(fmaxf(g, -L), L);
   u = fminf(fmaxf(u, -L), L);
@@ -140,7 +148,7 @@ __device__ __forceinline__ void epilogue_gemm1(uint32_t taddr, bool store, int64
       reg_fence16(u);
       float h[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) h[i] = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]), a.clamp);
+      for (int i = 0; i < 16; ++i) h[i] = silu_mul(lane_value(g[i], store), lane_value(u[i], store), a.clamp);
       uint32_t c[2];
       uint8_t sf;
       quant_nvfp4_16(h, c, sf);
@@ -168,7 +176,7 @@ __device__ __forceinline__ void epilogue_gemm1(uint32_t taddr, bool store, int64
         reg_fence16(u);
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          h[half * 16 + i] = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]), a.clamp);
+          h[half * 16 + i] = silu_mul(lane_value(g[i], store), lane_value(u[i], store), a.clamp);
       }
       uint32_t c[8];
       uint8_t sf;
@@ -192,8 +200,9 @@ __device__ __forceinline__ void epilogue_gemm1(uint32_t taddr, bool store, int64
       uint32_t o[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float h0 = silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), a.clamp);
-        const float h1 = silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]), a.clamp);
+        const float h0 = silu_mul(lane_value(g[2 * i], store), lane_value(u[2 * i], store), a.clamp);
+        const float h1 =
+            silu_mul(lane_value(g[2 * i + 1], store), lane_value(u[2 * i + 1], store), a.clamp);
         const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
         o[i] = *reinterpret_cast<const uint32_t*>(&b);
       }
