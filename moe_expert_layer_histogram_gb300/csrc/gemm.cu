@@ -123,10 +123,15 @@ __device__ __forceinline__ float lane_value(uint32_t bits, bool valid) {
   return valid ? __uint_as_float(bits) : 0.0f;
 }
 
+// silu(g) * u with the optional clamp.  Uses the hardware exp2 and
+// reciprocal approximations (__expf, __fdividef; a few ulp): the accurate
+// expf and IEEE division cost several microseconds per 16 features on the
+// one warp that holds a decode chunk, longer than a whole GEMM item.  For
+// g < -88, exp(-g) overflows to inf and the quotient is 0, as it should be.
 __device__ __forceinline__ float silu_mul(float g, float u, float L) {
   g = fminf(fmaxf(g, -L), L);
   u = fminf(fmaxf(u, -L), L);
-  return g / (1.0f + expf(-g)) * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // ---------------------------------------------------------------- epilogues
