@@ -45,6 +45,7 @@ struct moe_layer {
   uint8_t *h_in = nullptr, *o_out = nullptr;
   float* l_in = nullptr;
   GemmMaps maps1{}, maps2{};
+  int pair_scale_copies = 1;
   bool weights_ready = false;
   int last_T = 0, last_launches = 0;
   std::vector<cudaEvent_t> tev;  // per-kernel timing events, 7 per forward
@@ -111,6 +112,13 @@ void free_all(moe_layer* L) {
   L->allocs.clear();
 }
 
+// Chunks of at most 32 rows can take their block scales in with half as
+// many TMEM copies (lanes 0-31 only).  Measured on GB300 this speeds up
+// decode-sized launches (every chunk that small) by 10-15 %, but slows a
+// prefill launch that mixes such chunks with full ones (Zipf-routed T=8192:
+// GEMM2 +35 %), so it is used up to this many tokens.
+constexpr int kPairCopyMaxTokens = 1024;
+
 int64_t max_chunks(const moe_layer* L, int T) {
   const int64_t R = static_cast<int64_t>(T) * L->K;
   return std::min<int64_t>(L->E, R) + R / kRowBlock;
@@ -173,6 +181,7 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
     g_pdl_small = !(off == "1" || off == "small");
     g_pdl_gemm = !(off == "1" || off == "gemm");
   }
+  const char* pv = std::getenv("MOE_PAIR_SCALE_COPIES");
 
   moe_layer* L = new moe_layer;
   L->cfg = c;
@@ -188,6 +197,8 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   L->Rpad = Rpad;
   L->NBmax = (c.max_tokens + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
   L->clamp = (c.clamp_limit > 0.0f && std::isfinite(c.clamp_limit)) ? c.clamp_limit : INFINITY;
+  // MOE_PAIR_SCALE_COPIES=0 turns the decode-sized scale-copy path off.
+  L->pair_scale_copies = !(pv && pv[0] == '0');
   const int H = L->H, I = L->I, E = L->E;
   if (L->fmt == MOE_FMT_NVFP4) {
     L->xb = H / 2; L->hb = I / 2; L->x_tiles_k = H / 64; L->h_tiles_k = I / 64;
@@ -307,6 +318,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     a.out_sf = L->hsf;
     a.out_sf_tiles_k = L->h_tiles_k;
     a.clamp = L->clamp;
+    a.pair_scale_copies = L->pair_scale_copies && T <= kPairCopyMaxTokens;
     a.status = L->status;
     const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
     e = launch_gemm(L->fmt, 1, L->maps1, a, grid, T, s);
@@ -329,6 +341,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     a.out_sf = nullptr;
     a.out_sf_tiles_k = 0;
     a.clamp = INFINITY;
+    a.pair_scale_copies = L->pair_scale_copies && T <= kPairCopyMaxTokens;
     a.status = L->status;
     const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
     e = launch_gemm(L->fmt, 2, L->maps2, a, grid, T, s);

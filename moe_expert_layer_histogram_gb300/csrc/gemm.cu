@@ -360,6 +360,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++local) {
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
+        // A chunk of at most 32 rows keeps all its real accumulator rows in
+        // TMEM lane quarter 0.  The MMA of each lane quarter reads both
+        // operands' scales from that quarter's own lanes, so then only lanes
+        // 0-31 need correct scales: two 512-byte scale tiles go in with one
+        // non-broadcast 128x256b copy (the other lanes receive neighbouring
+        // shared memory and only feed accumulator rows that are not stored).
+        // Larger chunks broadcast every tile to all four quarters.
+        const bool q0_only =
+            args.pair_scale_copies && map_item(tab, args.E, args.n_tiles, item).rows <= 32;
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -377,22 +386,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sf = sp + A_BYTES + kTileBytes;  // weight scales, then activation scales
           const uint32_t sf_col = tmem + kSfColBase + stage * kSfColsPerStage;
           if constexpr (FMT == kFmtNVFP4) {
+            if (q0_only) {
+              // columns: A scales of substeps 0-1 | 2-3, B scales 0-1 | 2-3
+              const uint32_t sfa = smem_u32(sf + 4 * 512), sfb = smem_u32(sf);
+              tc_copy_128x256b(sf_col, desc_sf_pair(sfa, 512));
+              tc_copy_128x256b(sf_col + 8, desc_sf_pair(sfa + 1024, 512));
+              tc_copy_128x256b(sf_col + 16, desc_sf_pair(sfb, 512));
+              tc_copy_128x256b(sf_col + 24, desc_sf_pair(sfb + 1024, 512));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tc_copy_sf(sf_col + j * 8, desc_sf(smem_u32(sf + (4 + j) * 512)));
-              tc_copy_sf(sf_col + j * 8 + 4, desc_sf(smem_u32(sf + j * 512)));
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t c = (j >> 1) * 8 + (j & 1) * 4;
+                mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                         sf_col + c, sf_col + 16 + c, (kb | j) != 0);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                tc_copy_sf(sf_col + j * 8, desc_sf(smem_u32(sf + (4 + j) * 512)));
+                tc_copy_sf(sf_col + j * 8 + 4, desc_sf(smem_u32(sf + j * 512)));
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                         sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
+            }
+          } else if constexpr (FMT == kFmtMXFP8) {
+            if (q0_only) {
+              // columns 0-3: B scales, 4-7: A scales (tiles adjacent in smem)
+              tc_copy_128x256b(sf_col, desc_sf_pair(smem_u32(sf), 512));
+            } else {
+              tc_copy_sf(sf_col, desc_sf(smem_u32(sf)));
+              tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf + 512)));
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
-                       sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
-          } else if constexpr (FMT == kFmtMXFP8) {
-            tc_copy_sf(sf_col, desc_sf(smem_u32(sf + 512)));
-            tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf)));
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
               mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
-                       idesc_mxf8(128, 128, j), sf_col, sf_col + 4, (kb | j) != 0);
+                       idesc_mxf8(128, 128, j), sf_col + 4, sf_col, (kb | j) != 0);
           } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j)

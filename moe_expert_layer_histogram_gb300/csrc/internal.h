@@ -35,6 +35,7 @@ struct GemmArgs {
   uint8_t* out_sf;           // GEMM1 (MX/NV): GEMM2 input scales
   int out_sf_tiles_k;
   float clamp;               // +inf: no clamp
+  int pair_scale_copies;     // 1: chunks of <= 32 rows copy scales to lanes 0-31 only
   int* status;
 };
 

@@ -249,6 +249,18 @@ __device__ __forceinline__ void tc_copy_sf(uint32_t taddr, uint64_t sdesc) {
                : "memory");
 }
 
+// Copy a 128-row x 32-byte source (two 16-byte columns of 8-row x 16-byte
+// core matrices: rows 8 g.. at 128 g bytes, the second column lbo bytes
+// after the first) into TMEM: lane r receives row r's 32 bytes in 8
+// consecutive columns.  No broadcast: each lane quarter gets its own rows.
+__device__ __forceinline__ void tc_copy_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ uint64_t desc_sf_pair(uint32_t saddr, uint32_t lbo) {
+  return desc_sf(saddr) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16);
+}
+
 // Each thread of the warp reads 16 consecutive 32-bit columns of its TMEM
 // lane.  The registers are not valid until tmem_ld_wait(); reg_fence16()
 // after the wait re-defines them so no use can be scheduled before it.
