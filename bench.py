@@ -154,6 +154,57 @@ def algorithmic_bytes(s, counts):
     return {"gemm1_swiglu": g1, "gemm2": g2}, touched
 
 
+def ncu_traffic(s, touched, kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu captures
+    (profiles/gemm_traffic.json), scaled from the captured case to this run
+    by the number of touched experts (the weights dominate the traffic).
+    None when the workload was not captured or the kernel sources changed
+    since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    try:
+        tab = json.load(open(path))
+        for src, digest in tab["sources_sha1"].items():
+            with open(os.path.join(ROOT, src), "rb") as f:
+                if hashlib.sha1(f.read()).hexdigest() != digest:
+                    return None, "kernel changed since the ncu capture"
+        per = tab["per_touched_expert_bytes"][s["name"]][kernel]
+    except (OSError, KeyError, ValueError):
+        return None, "no ncu capture for this workload"
+    return int(per * touched), "ncu capture: " + tab["captures"][s["name"]] + \
+        ", scaled by touched experts"
+
+
+# ---------------------------------------------------------------- ranks
+def rank_env():
+    """(world, rank, local_rank) from the torchrun environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def max_over_ranks(x, device="cpu"):
+    """The largest value of x over all ranks (x itself on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, slowest_seconds):
+    """Replicas: every rank processes the same units; the job's rate is the
+    units of all ranks over the slowest rank's time."""
+    return units_per_rank * world / slowest_seconds
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args):
     import numpy as np
@@ -162,9 +213,7 @@ def run_ours(args):
 
     import moe_expert_layer_histogram_gb300 as moe
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -210,8 +259,7 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.5)
-    if world > 1:
-        dist.barrier()
+    barrier()
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -220,19 +268,15 @@ def run_ours(args):
         moe.moe_forward(layer.handle, hidden, logits, out, T, stream.cuda_stream)
     ev1.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    barrier()
     elapsed_ms = ev0.elapsed_time(ev1)
     clocks = sampler.stop()
     launches = moe.moe_last_launch_count(layer.handle) * steps
     st = layer.status()
     if st != 0:
         raise RuntimeError("device status %d after timed region" % st)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    value = T * steps * world / (elapsed_ms / 1e3)
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
+    value = whole_job_rate(T * steps, world, elapsed_ms / 1e3)
 
     # per-kernel durations: a second timed pass with CUDA events recorded
     # around every kernel (kept out of the pass above: events between kernels
@@ -254,6 +298,7 @@ def run_ours(args):
     roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
             "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "traffic": None, "algorithmic_bytes": alg[dom], "avg_launch_us": round(avg_ms * 1e3, 2)}
+    roof["traffic"], roof["traffic_source"] = ncu_traffic(s, touched, dom)
     layer_bytes = alg["gemm1_swiglu"] + alg["gemm2"]
     ms_step = elapsed_ms / steps
 
@@ -266,17 +311,12 @@ def run_ours(args):
         for _ in range(3):
             moe.moe_forward_host(layer.handle, hid_h, lg_h, out_h, T, stream.cuda_stream)
         e_steps = max(10, min(steps, 2000))
-        if world > 1:
-            dist.barrier()
+        barrier()
         t0 = time.perf_counter()
         for _ in range(e_steps):
             moe.moe_forward_host(layer.handle, hid_h, lg_h, out_h, T, stream.cuda_stream)
-        e_s = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_s = float(t.item())
-        e2e = {"value": round(T * e_steps * world / e_s, 1), "unit": "tokens/s",
+        e_s = max_over_ranks(time.perf_counter() - t0, dev)
+        e2e = {"value": round(whole_job_rate(T * e_steps, world, e_s), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": T * s["H"] * 2 + T * s["E"] * 4,
                "d2h_bytes_per_step": T * s["H"] * 2,
                "ms_per_step": round(e_s / e_steps * 1e3, 4)}
@@ -358,15 +398,14 @@ def run_reference(args):
     """The oracle as it stands, timed on the host cores.  Each step is one
     oracle forward over the first n tokens of the workload, n sized so the
     whole --warmup/--steps run stays within a few minutes."""
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    world, rank, _ = rank_env()
     if rank != 0:
         return
     import oracle
     import torch
     s = workload_spec(args)
     steps = args.steps or 3
-    warm = min(args.warmup, 1)
+    warm = args.warmup
     budget_core_s = 120.0 * oracle.num_threads() / max(1, steps + warm)
     n = max(1, min(cpu_sample_tokens(s, budget_core_s), s["T"]))
     dev = "cuda" if torch.cuda.is_available() else "cpu"
