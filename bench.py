@@ -299,8 +299,49 @@ def run_ours(args):
             "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "traffic": None, "algorithmic_bytes": alg[dom], "avg_launch_us": round(avg_ms * 1e3, 2)}
     roof["traffic"], roof["traffic_source"] = ncu_traffic(s, touched, dom)
+    roof["frac_of_8tbs"] = round(achieved / 8000.0, 4)
     layer_bytes = alg["gemm1_swiglu"] + alg["gemm2"]
     ms_step = elapsed_ms / steps
+
+    # the tensor-pipe side: the layer's FLOPs against this GPU's measured
+    # rate for the format's MMA kind (tcgen05 microbenchmark in the library)
+    flops = 6.0 * int(counts.sum()) * s["H"] * s["I"]
+    mma_peak = moe.moe_measure_mma_rate(s["fmt"], 256, iters=8000)
+    tensor = {"flops_per_step": flops,
+              "achieved_tflops": round(flops / (ms_step / 1e3) / 1e12, 1),
+              "peak_tflops": round(mma_peak, 1),
+              "peak_source": "measured: tcgen05.mma %s 128x256 loop on smem-resident operands"
+                             % s["fmt"],
+              "frac": round(flops / (ms_step / 1e3) / 1e12 / mma_peak, 4)}
+    binding_ms = max(layer_bytes / (peak * 1e9), flops / (mma_peak * 1e12)) * 1e3
+    tensor["binding_roofline_frac"] = round(binding_ms / ms_step, 4)
+
+    # the same forward captured once in a CUDA graph and replayed
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            moe.moe_forward(layer.handle, hidden, logits, out, T,
+                            torch.cuda.current_stream().cuda_stream)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        g_steps = max(10, min(steps, 2000))
+        gs0 = torch.cuda.Event(enable_timing=True)
+        gs1 = torch.cuda.Event(enable_timing=True)
+        gs0.record()
+        for _ in range(g_steps):
+            g.replay()
+        gs1.record()
+        torch.cuda.synchronize()
+        g_ms = gs0.elapsed_time(gs1) / g_steps
+        graph = {"value": round(whole_job_rate(T, world, g_ms / 1e3), 1), "unit": "tokens/s",
+                 "ms_per_step": round(g_ms, 5), "steps": g_steps}
+        del g
+    except Exception as exc:  # capture unsupported: report, do not fail the bench
+        graph = {"error": str(exc)[:200]}
+    if layer.status() != 0:
+        raise RuntimeError("device status %d after graph replay" % layer.status())
 
     # end to end: host buffers through the C ABI, copies inside the timed region
     e2e = None
@@ -342,6 +383,8 @@ def run_ours(args):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roof,
             "layer_hbm_frac": round(layer_bytes / (ms_step / 1e3) / 1e9 / peak, 4),
+            "tensor": tensor,
+            "graph": graph,
             "kernels_us": {k: round(v / max(nrec, 1) * 1e3, 2) for k, v in kern_ms.items()},
             "kernels_note": "per-kernel averages from a second pass of %d steps with events "
                             "around each kernel" % nrec,
@@ -375,7 +418,8 @@ def cpu_sample_tokens(s, core_seconds=20.0):
 
 
 def _cfg(s):
-    return dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"])
+    return dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"],
+                act=s.get("act", "swiglu"))
 
 
 def cpu_baseline(s, case, w_sample):

@@ -191,6 +191,22 @@ moe_status moe_route_permute_static(const float *router_logits, int T, int E,
                                     int32_t *offsets, int32_t *perm,
                                     void *stream);
 
+/* Tensor-pipe rate of one MMA kind on this GPU (measurement, not part of the
+ * layer): one CTA per SM issues `iters` groups of four back-to-back
+ * tcgen05.mma (M = 128, N = n_cols in {128, 256}) on zero operands resident
+ * in shared memory -- the layer's instruction shapes: kind::f16 (BF16,
+ * K = 16), kind::mxf8f6f4 block-scaled 1X (MXFP8, K = 32) or kind::mxf4nvf4
+ * block-scaled 4X (NVFP4, K = 64) -- and reports dense TFLOP/s in *tflops
+ * (host pointer), timed with CUDA events on `stream` (blocks until done).
+ * copy_scales != 0 (MXFP8/NVFP4, n_cols 128 only) also copies the scale
+ * tiles into TMEM before each group, as the layer's GEMM does per stage.
+ * The roofline of a block-scaled contraction needs this rate: the pages
+ * quote none for GB300.  Errors: MOE_ERR_INVALID_ARG (iters outside
+ * 1..2^20, bad format or n_cols), MOE_ERR_UNSUPPORTED, MOE_ERR_NO_DEVICE,
+ * MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT (a wait gave up after 2 s).        */
+moe_status moe_measure_mma_rate(int format, int n_cols, int copy_scales,
+                                int iters, double *tflops, void *stream);
+
 /* Static description of a status code (never NULL).                       */
 const char *moe_status_string(moe_status s);
 

@@ -39,7 +39,8 @@ class MoEError(RuntimeError):
 EXPORTS = ("moe_create", "moe_prepare_weights", "moe_forward", "moe_forward_host",
            "moe_debug_routing", "moe_debug_act_quant", "moe_debug_intermediates",
            "moe_get_status", "moe_timing_start", "moe_timing_stop", "moe_last_launch_count",
-           "moe_route_permute_static", "moe_status_string", "moe_destroy")
+           "moe_route_permute_static", "moe_measure_mma_rate", "moe_status_string",
+           "moe_destroy")
 
 _lib = None
 
@@ -65,6 +66,7 @@ def lib():
     L.moe_timing_stop.argtypes = [vp, vp, vp]
     L.moe_last_launch_count.argtypes = [vp]
     L.moe_route_permute_static.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp, vp]
+    L.moe_measure_mma_rate.argtypes = [ci, ci, ci, ci, ctypes.POINTER(ctypes.c_double), vp]
     L.moe_status_string.argtypes = [ci]
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_destroy.argtypes = [vp]
@@ -164,6 +166,16 @@ def moe_route_permute_static(router_logits, T, E, K, topk_ids, topk_w, offsets, 
     _check(lib().moe_route_permute_static(_ptr(router_logits), int(T), int(E), int(K),
                                           _ptr(topk_ids), _ptr(topk_w), _ptr(offsets),
                                           _ptr(perm), stream), "moe_route_permute_static")
+
+
+def moe_measure_mma_rate(fmt, n_cols=128, copy_scales=False, iters=20000, stream=None):
+    """Dense TFLOP/s of the layer's MMA kind for `fmt` on the current GPU
+    (tcgen05.mma on shared-memory-resident operands, one CTA per SM)."""
+    out = ctypes.c_double()
+    _check(lib().moe_measure_mma_rate(MOE_FMT[fmt] if isinstance(fmt, str) else int(fmt),
+                                      int(n_cols), int(bool(copy_scales)), int(iters),
+                                      ctypes.byref(out), stream), "moe_measure_mma_rate")
+    return out.value
 
 
 def moe_destroy(handle):

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmoe_gb300.so")
-SOURCES = ["gemm.cu", "route.cu", "prep.cu", "api.cu", "route_static.cu"]
+SOURCES = ["gemm.cu", "route.cu", "prep.cu", "api.cu", "route_static.cu", "peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

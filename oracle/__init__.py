@@ -15,6 +15,7 @@ from . import build as _build
 
 FMT_BF16, FMT_MXFP8, FMT_NVFP4 = 0, 1, 2
 FMT = {"bf16": FMT_BF16, "mxfp8": FMT_MXFP8, "nvfp4": FMT_NVFP4}
+ACT = {"swiglu": 0, "relu2": 1}
 
 _lib = None
 
@@ -22,7 +23,7 @@ _lib = None
 class _Cfg(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int),
                 ("K", ctypes.c_int), ("fmt", ctypes.c_int),
-                ("clamp", ctypes.c_float)]
+                ("clamp", ctypes.c_float), ("act", ctypes.c_int)]
 
 
 class _Weights(ctypes.Structure):
@@ -48,6 +49,8 @@ def lib():
                                   vp, vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.orc_token_forward.argtypes = [ctypes.POINTER(_Cfg),
                                         ctypes.POINTER(_Weights), vp, vp, vp, vp]
+        L.orc_forward_batched.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Weights),
+                                          vp, vp, ci, vp, vp]
         L.orc_num_threads.restype = ci
         L.orc_set_num_threads.argtypes = [ci]
         _lib = L
@@ -138,7 +141,7 @@ def permute(ids, E):
 # ---- the layer --------------------------------------------------------------
 def _pack(cfg, weights):
     c = _Cfg(cfg["H"], cfg["I"], cfg["E"], cfg["K"], FMT[cfg["fmt"]],
-             float(cfg.get("clamp", 0.0) or 0.0))
+             float(cfg.get("clamp", 0.0) or 0.0), ACT[cfg.get("act", "swiglu")])
     keep = {}
     ptrs = []
     for name in ("w13", "w13_sf", "w13_gs", "w2", "w2_sf", "w2_gs"):
@@ -194,6 +197,25 @@ def token_forward(cfg, weights, hidden_row, logits_row):
                                    _p(logits_row), _p(of), _p(ob)) == 0
     del keep
     return of, ob
+
+
+def forward_batched(cfg, weights, hidden, counts, want_y=False):
+    """Batched-expert format.  ``hidden``: uint16 bf16 bits [E,M,H];
+    ``counts``: int32 [E] (rows 0..counts[e]-1 of block e are expert e's).
+    Returns ``out`` uint16 [E,M,H] (rows past counts[e] zero) and, on
+    request, ``y`` float32 [E,M,H]."""
+    c, W, keep = _pack(cfg, weights)
+    hidden = _c(hidden, np.uint16)
+    counts = _c(counts, np.int32)
+    E, M, H = hidden.shape
+    res = {"out": np.zeros((E, M, H), np.uint16)}
+    if want_y:
+        res["y"] = np.zeros((E, M, H), np.float32)
+    rc = lib().orc_forward_batched(ctypes.byref(c), ctypes.byref(W), _p(hidden), _p(counts),
+                                   M, _p(res["out"]), _p(res.get("y")))
+    assert rc == 0, rc
+    del keep
+    return res
 
 
 def num_threads():

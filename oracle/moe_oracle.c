@@ -315,13 +315,19 @@ static void act_row(const orc_cfg *c, const uint16_t *hid, float *a,
     orc_dequant_row(c->fmt, codes, sf, H, a);
 }
 
+/* Rows of W13: gate and up (SwiGLU) or up only (ReLU^2). */
+static int w13_rows(const orc_cfg *c)
+{
+    return c->act == ORC_ACT_RELU2 ? c->I : 2 * c->I;
+}
+
 /* One dequantised weight row (exact in fp32).  which = 13: row n of W13_e
  * (reduction length H); which = 2: row n of W2_e (reduction length I).
  * NVFP4 block scales are first folded with the expert's global scale.   */
 static void weight_row(const orc_cfg *c, const orc_weights *wt, int which,
                        int e, int n, float *out, uint8_t *sf_tmp)
 {
-    int N = which == 13 ? 2 * c->I : c->H;
+    int N = which == 13 ? w13_rows(c) : c->H;
     int Kd = which == 13 ? c->H : c->I;
     size_t row = (size_t)e * N + n;
     const void *w = which == 13 ? wt->w13 : wt->w2;
@@ -355,14 +361,21 @@ static int clamp_on(const orc_cfg *c)
     return c->clamp > 0.0f && isfinite(c->clamp);
 }
 
-/* SwiGLU on one GEMM1 output row G[0..2I): gate = G[0..I), up = G[I..2I),
- * optional symmetric clamp of both, h = silu(gate) * up; then the GEMM2
- * input: bf16-rounded (BF16) or re-quantised per block from fp32 h.     */
+/* The activation on one GEMM1 output row.  SwiGLU: G[0..2I), gate =
+ * G[0..I), up = G[I..2I), optional symmetric clamp of both, h = silu(gate)
+ * * up.  ReLU^2: G[0..I), h = max(G, 0)^2.  Both in double, rounded to
+ * fp32.  Then the GEMM2 input: bf16-rounded (BF16) or re-quantised per
+ * block from fp32 h.                                                    */
 static void swiglu_requant(const orc_cfg *c, const float *G, float *hq,
                            uint8_t *codes, uint8_t *sf)
 {
     int I = c->I;
-    for (int i = 0; i < I; i++) {
+    for (int i = 0; i < I && c->act == ORC_ACT_RELU2; i++) {
+        /* non-gated squared ReLU of the single projection */
+        double g = G[i] > 0.0f ? (double)G[i] : 0.0;
+        hq[i] = (float)(g * g);
+    }
+    for (int i = 0; i < I && c->act == ORC_ACT_SWIGLU; i++) {
         float g = G[i], u = G[I + i];
         if (clamp_on(c)) {
             float L = c->clamp;
@@ -390,6 +403,10 @@ static int check_cfg(const orc_cfg *c)
     if (c->fmt == ORC_FMT_NVFP4 && (c->H % 16 || c->I % 16))
         return -1;
     if (c->fmt == ORC_FMT_MXFP8 && (c->H % 32 || c->I % 32))
+        return -1;
+    if (c->act != ORC_ACT_SWIGLU && c->act != ORC_ACT_RELU2)
+        return -1;
+    if (c->act == ORC_ACT_RELU2 && clamp_on(c))
         return -1;
     return 0;
 }
@@ -442,7 +459,8 @@ int orc_forward(const orc_cfg *c, const orc_weights *wt,
     for (int e = 0; e < E; e++)
         if (off[e + 1] - off[e] > maxrows)
             maxrows = off[e + 1] - off[e];
-    G = (float *)malloc(sizeof(float) * (size_t)maxrows * 2 * I + 1);
+    const int N1 = w13_rows(c);
+    G = (float *)malloc(sizeof(float) * (size_t)maxrows * N1 + 1);
 
     /* 4. expert by expert: GEMM1, SwiGLU + re-quantisation, GEMM2 */
     for (int e = 0; e < E; e++) {
@@ -455,16 +473,16 @@ int orc_forward(const orc_cfg *c, const orc_weights *wt,
             uint8_t *sft = (uint8_t *)malloc((size_t)(H > I ? H : I) / 16 + 1);
             uint8_t *qc = (uint8_t *)malloc((size_t)hb + hs + 1);
 #pragma omp for schedule(static)
-            for (int n = 0; n < 2 * I; n++) {
+            for (int n = 0; n < N1; n++) {
                 weight_row(c, wt, 13, e, n, wrow, sft);
                 for (int r = 0; r < nr; r++) {
                     int t = perm[r0 + r] / K;
-                    G[(size_t)r * 2 * I + n] = dot(A + (size_t)t * H, wrow, H);
+                    G[(size_t)r * N1 + n] = dot(A + (size_t)t * H, wrow, H);
                 }
             }
 #pragma omp for schedule(static)
             for (int r = 0; r < nr; r++)
-                swiglu_requant(c, G + (size_t)r * 2 * I,
+                swiglu_requant(c, G + (size_t)r * N1,
                                Hq + (size_t)(r0 + r) * I, qc, qc + hb);
 #pragma omp for schedule(static)
             for (int j = 0; j < H; j++) {
@@ -530,7 +548,7 @@ int orc_token_forward(const orc_cfg *c, const orc_weights *wt,
             float *wrow = (float *)malloc(sizeof(float) * (H > I ? H : I));
             uint8_t *sft = (uint8_t *)malloc((size_t)(H > I ? H : I) / 16 + 1);
 #pragma omp for schedule(static)
-            for (int n = 0; n < 2 * I; n++) {
+            for (int n = 0; n < w13_rows(c); n++) {
                 weight_row(c, wt, 13, e, n, wrow, sft);
                 G[n] = dot(a, wrow, H);
             }
@@ -560,6 +578,65 @@ int orc_token_forward(const orc_cfg *c, const orc_weights *wt,
     free(hq);
     free(acc);
     free(qc);
+    return 0;
+}
+
+int orc_forward_batched(const orc_cfg *c, const orc_weights *wt,
+                        const uint16_t *hidden, const int32_t *counts, int M,
+                        uint16_t *out, float *y)
+{
+    if (check_cfg(c) || M < 0)
+        return -1;
+    const int H = c->H, I = c->I, E = c->E, fmt = c->fmt, N1 = w13_rows(c);
+    const int xb = bytes_per_row(fmt, H), hb = bytes_per_row(fmt, I);
+    const int hs = sf_per_row(fmt, I);
+    for (int e = 0; e < E; e++)
+        if (counts[e] < 0 || counts[e] > M)
+            return -1;
+    for (int e = 0; e < E; e++) {
+        const int nr = counts[e];
+        if (nr == 0)
+            continue;
+        float *A = (float *)malloc(sizeof(float) * (size_t)nr * H);
+        float *G = (float *)malloc(sizeof(float) * (size_t)nr * N1);
+        float *Hq = (float *)malloc(sizeof(float) * (size_t)nr * I);
+#pragma omp parallel
+        {
+            float *wrow = (float *)malloc(sizeof(float) * (H > I ? H : I));
+            uint8_t *sft = (uint8_t *)malloc((size_t)(H > I ? H : I) / 16 + 1);
+            uint8_t *qc = (uint8_t *)malloc((size_t)(xb > hb ? xb : hb) + H / 16 + hs + 1);
+#pragma omp for schedule(static)
+            for (int r = 0; r < nr; r++)
+                act_row(c, hidden + ((size_t)e * M + r) * H, A + (size_t)r * H, qc,
+                        qc + xb);
+#pragma omp for schedule(static)
+            for (int n = 0; n < N1; n++) {
+                weight_row(c, wt, 13, e, n, wrow, sft);
+                for (int r = 0; r < nr; r++)
+                    G[(size_t)r * N1 + n] = dot(A + (size_t)r * H, wrow, H);
+            }
+#pragma omp for schedule(static)
+            for (int r = 0; r < nr; r++)
+                swiglu_requant(c, G + (size_t)r * N1, Hq + (size_t)r * I, qc, qc + hb);
+#pragma omp for schedule(static)
+            for (int j = 0; j < H; j++) {
+                weight_row(c, wt, 2, e, j, wrow, sft);
+                for (int r = 0; r < nr; r++) {
+                    const float v = dot(Hq + (size_t)r * I, wrow, I);
+                    const size_t o = ((size_t)e * M + r) * H + j;
+                    out[o] = orc_f32_to_bf16(v);
+                    if (y)
+                        y[o] = v;
+                }
+            }
+            free(wrow);
+            free(sft);
+            free(qc);
+        }
+        free(A);
+        free(G);
+        free(Hq);
+    }
     return 0;
 }
 

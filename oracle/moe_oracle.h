@@ -10,8 +10,9 @@
  *   top-k routing with a softmax over the selected logits, a stable counting
  *   sort of the (token, k) slots into expert-contiguous order, per-expert
  *   W13 GEMM on exactly dequantised operands, SwiGLU with optional gate/up
- *   clamp, re-quantisation of the GEMM2 input, per-expert W2 GEMM and the
- *   routing-weighted top-k combine.  Sources:
+ *   clamp (or the non-gated ReLU^2), re-quantisation of the GEMM2 input,
+ *   per-expert W2 GEMM and the routing-weighted top-k combine; and the same
+ *   expert computation on the batched-expert input format.  Sources:
  *     - "PR #40082 report: Integrate flashinfer b12x MoE and FP4 GEMM kernels
  *       for SM120/121" (prhub.com.cn), sec. 实现拆解 item 1: the layer's steps
  *       (routing, the gate/up GEMM, SwiGLU, the down GEMM, the reduction)
@@ -26,6 +27,12 @@
  *       NVFP4 blocks of 16 (nvfp4_quantize_per_block_16), MXFP8 blocks of 32
  *       (mxfp8_quantize_per_block_32), and sec. 三 (comm.py): an optional
  *       gate/up clamp (resolve_gate_up_clamp).
+ *     - same PR #40082 page, sec. 风险与影响 item 4: MoE models without a
+ *       gated act-and-mul MLP, such as Nemotron's ReLU^2 experts.
+ *     - "PR 38050 analysis report" (prhub.com.cn, vLLM PR 38050), sec.
+ *       实现拆解: the batched-experts variant that takes activations already
+ *       grouped per expert ([E, max tokens per expert, H] plus per-expert
+ *       counts) and returns the expert outputs in the same layout.
  *   The element formats themselves (e2m1, e4m3 "fn", e8m0, bf16) are the
  *   public OCP Microscaling v1.0 / OCP 8-bit float definitions.
  *
@@ -88,9 +95,14 @@ void orc_permute(const int32_t *ids, int T, int K, int E, int32_t *offsets,
                  int32_t *perm, int32_t *inv);
 
 /* ---- the layer -------------------------------------------------------- */
+enum { ORC_ACT_SWIGLU = 0, ORC_ACT_RELU2 = 1 };
+
 typedef struct {
     int H, I, E, K, fmt;
     float clamp;          /* > 0 and finite: clamp gate and up to [-L, L] */
+    int act;              /* ORC_ACT_SWIGLU (gated, W13 has 2I rows) or
+                             ORC_ACT_RELU2 (non-gated, W13 has I rows:
+                             h = max(G, 0)^2; no clamp)                  */
 } orc_cfg;
 
 /* Canonical weights (row-major, reduction dim contiguous):
@@ -98,7 +110,9 @@ typedef struct {
  *   MXFP8: w13 e4m3 [E,2I,H], w13_sf e8m0 [E,2I,H/32]; w2 [E,H,I], [E,H,I/32]
  *   NVFP4: w13 u8 [E,2I,H/2], w13_sf e4m3 [E,2I,H/16], w13_gs f32 [E];
  *          w2 u8 [E,H,I/2], w2_sf e4m3 [E,H,I/16], w2_gs f32 [E]
- * Rows 0..I-1 of W13 are the gate projection, rows I..2I-1 the up one.    */
+ * Rows 0..I-1 of W13 are the gate projection, rows I..2I-1 the up one.
+ * With ORC_ACT_RELU2, W13 is the single up projection [E,I,H] (likewise for
+ * its scales).                                                             */
 typedef struct {
     const void *w13; const uint8_t *w13_sf; const float *w13_gs;
     const void *w2;  const uint8_t *w2_sf;  const float *w2_gs;
@@ -121,6 +135,16 @@ int orc_forward(const orc_cfg *cfg, const orc_weights *wt,
 int orc_token_forward(const orc_cfg *cfg, const orc_weights *wt,
                       const uint16_t *hidden_row, const float *logits_row,
                       float *out_f32, uint16_t *out);
+
+/* Batched-expert format: no routing, permutation or combine.  hidden bf16
+ * [E,M,H]: expert e's rows are rows 0..counts[e]-1 of block e (counts[e]
+ * <= M).  Each such row goes through GEMM1 input quantisation, GEMM1, the
+ * activation with re-quantisation and GEMM2 of expert e; out bf16 [E,M,H]
+ * receives bf16(GEMM2 output) in the same rows (other rows are left as
+ * they are); y (optional) the fp32 GEMM2 output.  Returns 0 or -1.       */
+int orc_forward_batched(const orc_cfg *cfg, const orc_weights *wt,
+                        const uint16_t *hidden, const int32_t *counts, int M,
+                        uint16_t *out, float *y);
 
 /* Bulk codec helpers (tests): kind 0 bf16 (uint16 codes), 1 e4m3,
  * 2 e2m1 (one code per byte), 3 e8m0.  Encoding e8m0 is not defined.  */

@@ -9,7 +9,8 @@ TOL = {"bf16": 5e-3, "mxfp8": 2e-2, "nvfp4": 2e-2}
 
 
 def cfg_of(s):
-    return dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"])
+    return dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"],
+                act=s.get("act", "swiglu"))
 
 
 def rel_l2(a, b):

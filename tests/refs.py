@@ -81,31 +81,44 @@ def dequant_weights(fmt, w, sf=None, gs=None):
     return v * e4m3_value(folded).repeat_interleave(16, dim=-1)
 
 
-def dense_layer_f64(fmt, clamp, hidden_bits, logits, W13, W2, weights_k):
-    """Top-k routed layer written densely: for each token, every selected
-    expert's output weighted by the renormalised softmax.  fp32 roundings
-    mirror the layer's: GEMM results and h are rounded to fp32 before the
-    GEMM2-input quantisation.  Returns float64 [T, H] (before bf16)."""
+def expert_mlp_f64(fmt, clamp, a, W13e, W2e, act="swiglu"):
+    """One expert on one dequantised GEMM1 input row ``a`` (float64 [H]).
+    fp32 roundings mirror the layer's: the GEMM results and h are rounded
+    to fp32 before the GEMM2-input quantisation.  Returns float64 [H] (the
+    fp32 GEMM2 output)."""
+    G = (W13e @ a).to(torch.float32)
+    if act == "relu2":
+        h = (torch.relu(G.to(torch.float64)) ** 2).to(torch.float32)
+    else:
+        I = G.shape[0] // 2
+        g, u = G[:I], G[I:]
+        if clamp and clamp > 0:
+            g = g.clamp(-clamp, clamp)
+            u = u.clamp(-clamp, clamp)
+        h = (torch.nn.functional.silu(g.to(torch.float64)) * u.to(torch.float64)).to(torch.float32)
+    hq = quant_dequant(fmt, h.unsqueeze(0))[0]
+    return (W2e @ hq).to(torch.float32).to(torch.float64)
+
+
+def gemm1_input_f64(fmt, hidden_bits):
     x = torch.as_tensor(np.asarray(hidden_bits)).view(torch.int16).view(torch.bfloat16).to(torch.float32)
-    a = quant_dequant(fmt, x) if fmt != "bf16" else x.to(torch.float64)
+    return quant_dequant(fmt, x) if fmt != "bf16" else x.to(torch.float64)
+
+
+def dense_layer_f64(fmt, clamp, hidden_bits, logits, W13, W2, weights_k, act="swiglu"):
+    """Top-k routed layer written densely: for each token, every selected
+    expert's output weighted by the renormalised softmax.  Returns float64
+    [T, H] (before bf16)."""
+    a = gemm1_input_f64(fmt, hidden_bits)
     lg = torch.as_tensor(np.asarray(logits)).to(torch.float64)
-    T = x.shape[0]
-    I = W13.shape[1] // 2
+    T = a.shape[0]
     top = torch.topk(lg, weights_k, dim=-1)
     p = torch.softmax(top.values, -1)
     out = torch.zeros(T, W2.shape[1], dtype=torch.float64)
     for t in range(T):
         for j in range(weights_k):
             e = int(top.indices[t, j])
-            G = (W13[e] @ a[t]).to(torch.float32)
-            g, u = G[:I], G[I:]
-            if clamp and clamp > 0:
-                g = g.clamp(-clamp, clamp)
-                u = u.clamp(-clamp, clamp)
-            h = (torch.nn.functional.silu(g.to(torch.float64)) * u.to(torch.float64)).to(torch.float32)
-            hq = quant_dequant(fmt, h.unsqueeze(0))[0]
-            y = (W2[e] @ hq).to(torch.float32).to(torch.float64)
-            out[t] += p[t, j] * y
+            out[t] += p[t, j] * expert_mlp_f64(fmt, clamp, a[t], W13[e], W2[e], act)
     return out
 
 

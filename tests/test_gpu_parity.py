@@ -170,3 +170,48 @@ def test_allocation_failure_reports_oom_and_frees(monkeypatch):
     moe_destroy(h)
     torch.cuda.synchronize()
     assert abs(torch.cuda.mem_get_info()[0] - free0) < (64 << 20)
+
+
+def test_forward_replays_from_a_cuda_graph():
+    # the forward allocates nothing and never syncs the host, so it can be
+    # captured once and replayed on new inputs written into the same buffers
+    from moe_expert_layer_histogram_gb300 import moe_forward
+    s = workloads.spec("nvfp4_small")
+    case = workloads.make_case(s, seed=4)
+    case2 = workloads.make_case(s, seed=6, weights=False)
+    layer = make_layer(s, weights=case["weights"])
+    hid, lg = case["hidden"].cuda(), case["logits"].cuda()
+    ref1 = run_gpu(layer, hid, lg).clone()
+    ref2 = run_gpu(layer, case2["hidden"].cuda(), case2["logits"].cuda()).clone()
+    out = torch.empty_like(hid)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe_forward(layer.handle, hid, lg, out, s["T"], torch.cuda.current_stream().cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref1)
+    hid.copy_(case2["hidden"])
+    lg.copy_(case2["logits"])
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref2)
+    assert layer.status() == 0
+    layer.close()
+
+
+def test_mma_rate_measurement():
+    import json
+    import os
+    from moe_expert_layer_histogram_gb300 import moe_measure_mma_rate
+    bf16 = moe_measure_mma_rate("bf16", 256, iters=4000)
+    peaks = os.path.join(os.path.dirname(os.path.dirname(__file__)), "MEASURED_PEAKS.json")
+    ref = 2250.0
+    if os.path.exists(peaks):
+        ref = json.load(open(peaks)).get("bf16_tflops", ref) or ref
+    # the tensor pipe's BF16 rate is of the order of a large cuBLAS GEMM's
+    assert 0.5 * ref < bf16 < 1.6 * ref, (bf16, ref)
+    fp8 = moe_measure_mma_rate("mxfp8", 256, iters=4000)
+    fp4 = moe_measure_mma_rate("nvfp4", 256, iters=4000)
+    assert fp8 > 1.5 * bf16 and fp4 > 1.5 * fp8, (bf16, fp8, fp4)
+    with_copies = moe_measure_mma_rate("nvfp4", 128, copy_scales=True, iters=4000)
+    assert 0 < with_copies

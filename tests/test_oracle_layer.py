@@ -22,7 +22,8 @@ def _case(name, seed=0, **over):
 
 
 def _cfg(s):
-    return dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"])
+    return dict(H=s["H"], I=s["I"], E=s["E"], K=s["K"], fmt=s["fmt"], clamp=s["clamp"],
+                act=s.get("act", "swiglu"))
 
 
 TINY = [
@@ -121,3 +122,94 @@ def test_intermediates_shapes_and_activation_codes():
     codes, sf = oracle.quant_row("nvfp4", x)
     assert np.array_equal(res["xq_codes"], codes) and np.array_equal(res["xq_sf"], sf)
     assert res["h"].shape == (10, 32) and res["y"].shape == (10, 64)
+
+
+# ---- the non-gated ReLU^2 activation ---------------------------------------
+RELU2 = [
+    ("bf16_small", dict(T=10, H=128, I=64, E=5, K=2, clamp=0.0, act="relu2")),
+    ("mxfp8_small", dict(T=9, H=128, I=64, E=4, K=2, act="relu2")),
+    ("nvfp4_small", dict(T=11, H=128, I=64, E=6, K=3, act="relu2")),
+]
+
+
+@pytest.mark.parametrize("name,over", RELU2, ids=[t[0] for t in RELU2])
+def test_relu2_layer_vs_restatement_and_brute_force(name, over):
+    s, c = _case(name, seed=8, **over)
+    cfg = _cfg(s)
+    assert c["weights"]["w13"].shape[1] == s["I"]          # one projection, I rows
+    W13, W2 = _dequant(s, c["weights"])
+    ref = refs.dense_layer_f64(s["fmt"], 0.0, c["hidden"], c["logits"], W13, W2, s["K"],
+                               act="relu2")
+    res = oracle.forward(cfg, c["weights"], c["hidden"], c["logits"])
+    assert refs.rel_l2(refs.bf16_bits_to_f32(res["out"]), ref.numpy()) < 4e-3
+    for t in range(c["hidden"].shape[0]):
+        of, ob = oracle.token_forward(cfg, c["weights"], c["hidden"][t], c["logits"][t])
+        assert np.array_equal(ob, res["out"][t]), t
+        assert refs.rel_l2(of, ref[t].numpy()) < 2e-6, t
+
+
+def test_relu2_is_not_swiglu_and_is_nonnegative_before_gemm2():
+    # h = max(G, 0)^2 >= 0 (a sign or gating mistake shows up here)
+    s, c = _case("bf16_small", seed=2, T=6, H=64, I=32, E=3, K=2, clamp=0.0, act="relu2")
+    res = oracle.forward(_cfg(s), c["weights"], c["hidden"], c["logits"],
+                         want_intermediates=True)
+    assert (res["h"] >= 0).all() and (res["h"] == 0).any() and (res["h"] > 0).any()
+
+
+def test_relu2_rejects_clamp():
+    s, c = _case("bf16_small", T=4, H=64, I=32, E=3, K=2, clamp=0.0, act="relu2")
+    cfg = dict(_cfg(s), clamp=3.0)
+    with pytest.raises(AssertionError):
+        oracle.forward(cfg, c["weights"], c["hidden"], c["logits"])
+
+
+# ---- the batched-expert format ----------------------------------------------
+BATCHED = [
+    ("bf16_small", dict(H=128, I=64, E=4, clamp=0.5), 5),
+    ("mxfp8_small", dict(H=128, I=64, E=4), 6),
+    ("nvfp4_small", dict(H=128, I=64, E=5), 7),
+    ("nvfp4_small", dict(H=128, I=64, E=4, act="relu2"), 3),
+]
+
+
+@pytest.mark.parametrize("name,over,M", BATCHED, ids=["%s-%d" % (b[0], i) for i, b in enumerate(BATCHED)])
+def test_batched_format_vs_restatement(name, over, M):
+    import torch
+    s = workloads.spec(name, **over)
+    w = workloads.to_numpy_case(workloads.make_case(s, T=1, seed=4))["weights"]
+    hid, counts = workloads.draw_batched(s, M, seed=4)
+    hb = hid.view(torch.int16).numpy().view("uint16")
+    cn = counts.numpy()
+    assert cn[0] == 0 and cn[1] == M and cn[2] == 1
+    res = oracle.forward_batched(_cfg(s), w, hb, cn, want_y=True)
+    W13, W2 = _dequant(s, w)
+    for e in range(s["E"]):
+        for r in range(M):
+            if r >= cn[e]:
+                assert not res["out"][e, r].any()        # rows past the count untouched
+                continue
+            a = refs.gemm1_input_f64(s["fmt"], hb[e, r:r + 1])[0]
+            y = refs.expert_mlp_f64(s["fmt"], s["clamp"], a, W13[e], W2[e], s["act"])
+            assert refs.rel_l2(res["y"][e, r], y.numpy()) < 2e-6, (e, r)
+    # the output is the bf16 rounding of y
+    y32 = torch.from_numpy(res["y"])
+    assert np.array_equal(y32.to(torch.bfloat16).view(torch.int16).numpy().view("uint16"),
+                          res["out"])
+
+
+def test_batched_rows_match_the_routed_layer_rows():
+    # a batched call whose rows are the routed layer's permuted rows gives
+    # that layer's GEMM2 output row for row
+    s, c = _case("mxfp8_small", seed=5, T=7, H=128, I=64, E=4, K=2)
+    cfg = _cfg(s)
+    res = oracle.forward(cfg, c["weights"], c["hidden"], c["logits"], want_intermediates=True)
+    off, perm = res["offsets"], res["perm"]
+    counts = np.diff(off).astype(np.int32)
+    M = int(counts.max())
+    hid = np.zeros((s["E"], M, s["H"]), np.uint16)
+    for e in range(s["E"]):
+        for r in range(counts[e]):
+            hid[e, r] = c["hidden"][perm[off[e] + r] // s["K"]]
+    b = oracle.forward_batched(cfg, c["weights"], hid, counts, want_y=True)
+    for e in range(s["E"]):
+        assert np.array_equal(b["y"][e, :counts[e]], res["y"][off[e]:off[e + 1]])

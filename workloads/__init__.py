@@ -57,10 +57,18 @@ SMALL = {
 
 
 def spec(name, **over):
+    """Layer shape and input recipe.  ``act`` is the expert activation:
+    "swiglu" (gated; W13 holds gate and up, 2I rows) unless overridden with
+    "relu2" (non-gated squared ReLU; W13 holds the I rows of one projection)."""
     d = dict(CONFIGS.get(name) or SMALL[name])
+    d.setdefault("act", "swiglu")
     d.update(over)
     d["name"] = name
     return d
+
+
+def w13_rows(s):
+    return s["I"] if s.get("act", "swiglu") == "relu2" else 2 * s["I"]
 
 
 # ---------------------------------------------------------------------------
@@ -162,10 +170,11 @@ def _expert_gen(seed, which, e, device):
 
 
 def draw_expert(s, which, e, seed, device):
-    """One expert's canonical matrix: W13_e [2I, H] or W2_e [H, I] (bf16), or
-    its quantised codes, block scales and (NVFP4) global scale."""
+    """One expert's canonical matrix: W13_e [2I, H] (or [I, H] for ReLU^2)
+    or W2_e [H, I] (bf16), or its quantised codes, block scales and (NVFP4)
+    global scale."""
     H, I, fmt = s["H"], s["I"], s["fmt"]
-    rows_in, cols_out = (H, 2 * I) if which == "w13" else (I, H)
+    rows_in, cols_out = (H, w13_rows(s)) if which == "w13" else (I, H)
     std = (1.0 / math.sqrt(rows_in)) if s["wdist"] == "fan_in" else float(s["wdist"])
     g = _expert_gen(seed, which, e, device)
     x = (torch.randn(rows_in, cols_out, generator=g, device=device,
@@ -184,7 +193,7 @@ def weight_shapes(s):
     """name -> (shape, torch dtype) of the canonical weight arrays."""
     E, H, I, fmt = s["E"], s["H"], s["I"], s["fmt"]
     out = {}
-    for which, (N, K) in (("w13", (2 * I, H)), ("w2", (H, I))):
+    for which, (N, K) in (("w13", (w13_rows(s), H)), ("w2", (H, I))):
         if fmt == "bf16":
             out[which] = ((E, N, K), torch.bfloat16)
         elif fmt == "nvfp4":
@@ -199,7 +208,8 @@ def weight_shapes(s):
 
 def draw_weights(s, seed, device):
     """Canonical weights of all experts: W13 [E, 2I, H] (rows 0..I-1 gate,
-    I..2I-1 up) and W2 [E, H, I], reduction dim contiguous.  Each expert
+    I..2I-1 up; [E, I, H] for ReLU^2) and W2 [E, H, I], reduction dim
+    contiguous.  Each expert
     matrix is drawn in the input-major shape ([H, 2I] / [I, H]), transposed
     and, for MXFP8/NVFP4, quantised."""
     out = {k: torch.empty(shape, dtype=dt, device=device)
@@ -247,6 +257,22 @@ def make_case(s, T=None, seed=0, device="cpu", weights=True):
     if weights:
         case["weights"] = draw_weights(s, seed, device)
     return case
+
+
+def draw_batched(s, M, seed=0, device="cpu"):
+    """Batched-expert input: bf16 hidden [E, M, H] N(0,1) and int32 counts
+    [E] with rows 0..counts[e]-1 of block e valid.  Counts are uniform in
+    [0, M], with expert 0 empty, expert 1 full (M rows) and expert 2 holding
+    one row whenever E > 2; rows past a count hold N(0,1) values too (they
+    must be ignored)."""
+    g = _gen(seed * 7919 + 17, device)
+    E, H = s["E"], s["H"]
+    counts = torch.randint(0, M + 1, (E,), generator=g, device=device, dtype=torch.int32)
+    if E > 2 and M > 0:
+        counts[0], counts[1], counts[2] = 0, M, 1
+    hidden = torch.randn(E, M, H, generator=g, device=device,
+                         dtype=torch.float32).to(torch.bfloat16).contiguous()
+    return hidden, counts
 
 
 def forced_empty_logits(logits, experts):
