@@ -43,6 +43,8 @@ def parse_args():
     p.add_argument("--tokens", type=int, default=0, help="override T (decode sweep)")
     p.add_argument("--experts", type=int, default=0,
                    help="override E (small cases for profiler captures)")
+    p.add_argument("--act", default="", choices=["", "swiglu", "relu2"],
+                   help="expert activation (default: the workload's; relu2 drops the clamp)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -55,12 +57,16 @@ def workload_spec(args):
         s["T"] = args.tokens
     if args.experts:
         s["E"] = args.experts
+    if args.act:
+        s["act"] = args.act
+        if args.act == "relu2":
+            s["clamp"] = 0.0
     return s
 
 
 def describe(s):
-    return "%s: T=%d H=%d I=%d E=%d top-%d %s%s, logits %s" % (
-        s["name"], s["T"], s["H"], s["I"], s["E"], s["K"], s["fmt"],
+    return "%s: T=%d H=%d I=%d E=%d top-%d %s %s%s, logits %s" % (
+        s["name"], s["T"], s["H"], s["I"], s["E"], s["K"], s["fmt"], s.get("act", "swiglu"),
         (", clamp %g" % s["clamp"]) if s["clamp"] else "", s["logits"])
 
 
@@ -149,7 +155,7 @@ def algorithmic_bytes(s, counts):
     else:
         wb = lambda n, k: 2 * n * k                         # noqa: E731
         ab = lambda k: 2 * k                                # noqa: E731
-    g1 = touched * wb(2 * I, H) + R * ab(H) + R * ab(I)
+    g1 = touched * wb(workloads.w13_rows(s), H) + R * ab(H) + R * ab(I)
     g2 = touched * wb(H, I) + R * ab(I) + R * 2 * H
     return {"gemm1_swiglu": g1, "gemm2": g2}, touched
 
@@ -222,7 +228,7 @@ def run_ours(args):
     T = s["T"]
 
     case = workloads.make_case(s, seed=0, device=dev)
-    layer = moe.MoELayer(T, s["H"], s["I"], s["E"], s["K"], s["fmt"], s["clamp"])
+    layer = moe.MoELayer(T, s["H"], s["I"], s["E"], s["K"], s["fmt"], s["clamp"], s["act"])
     layer.prepare_weights(case["weights"])
     torch.cuda.synchronize()
     w_sample = None
@@ -305,7 +311,7 @@ def run_ours(args):
 
     # the tensor-pipe side: the layer's FLOPs against this GPU's measured
     # rate for the format's MMA kind (tcgen05 microbenchmark in the library)
-    flops = 6.0 * int(counts.sum()) * s["H"] * s["I"]
+    flops = 2.0 * int(counts.sum()) * s["H"] * (workloads.w13_rows(s) + s["I"])
     mma_peak = moe.moe_measure_mma_rate(s["fmt"], 256, iters=8000)
     tensor = {"flops_per_step": flops,
               "achieved_tflops": round(flops / (ms_step / 1e3) / 1e12, 1),

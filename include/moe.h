@@ -67,6 +67,12 @@ typedef enum {
 
 typedef enum { MOE_FMT_BF16 = 0, MOE_FMT_MXFP8 = 1, MOE_FMT_NVFP4 = 2 } moe_format;
 
+/* Expert activation.  SwiGLU is gated (W13 = gate and up projections);
+ * ReLU^2 is the non-gated squared ReLU of one projection, h = max(x, 0)^2,
+ * which the b12x backend cannot load (PR #40082 report, sec. 风险与影响
+ * item 4: models without a gated act-and-mul MLP, e.g. Nemotron).        */
+typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_RELU2 = 1 } moe_activation;
+
 typedef struct {
     int max_tokens;    /* T_max: largest T any forward will use (>= 1)       */
     int hidden;        /* H: multiple of 128 (NVFP4: of 256)                 */
@@ -75,7 +81,9 @@ typedef struct {
     int top_k;         /* K: 1..min(E, 16)                                   */
     int format;        /* moe_format                                         */
     float clamp_limit; /* L > 0 and finite: clamp gate and up to [-L, L]
-                          before silu(gate)*up; otherwise no clamp          */
+                          before silu(gate)*up; otherwise no clamp (a clamp
+                          with MOE_ACT_RELU2 is MOE_ERR_UNSUPPORTED)        */
+    int activation;    /* moe_activation (0 = SwiGLU)                       */
 } moe_config;
 
 typedef struct moe_layer moe_layer;   /* opaque */
@@ -93,7 +101,8 @@ moe_status moe_create(const moe_config *cfg, moe_layer **out);
  * after enqueueing, the caller may free its buffers once `stream` has
  * finished).  All pointers are device pointers, row-major, reduction
  * dimension contiguous; W13 rows 0..I-1 are the gate projection and rows
- * I..2I-1 the up projection:
+ * I..2I-1 the up projection (MOE_ACT_RELU2: W13 is the single projection,
+ * I rows, so every "2I" below reads "I"):
  *   BF16 : w13 bf16 [E, 2I, H];  w2 bf16 [E, H, I];  *_sf, *_gs unused.
  *   MXFP8: w13 e4m3 [E, 2I, H], w13_sf e8m0 [E, 2I, H/32];
  *          w2  e4m3 [E, H, I],  w2_sf  e8m0 [E, H, I/32];  *_gs unused.
@@ -120,6 +129,25 @@ moe_status moe_prepare_weights(moe_layer *layer,
 moe_status moe_forward(moe_layer *layer, const void *hidden,
                        const float *router_logits, void *out, int T,
                        void *stream);
+
+/* The expert computation on the batched-expert activation format: no
+ * routing, permutation or combine (the batched-experts variant of PR 38050
+ * analysis report, sec. 实现拆解: activations already grouped per expert,
+ * a per-expert token count, outputs in the same layout).  hidden: device
+ * bf16 [E, M, H]; counts: device int32 [E], rows 0..counts[e]-1 of block e
+ * belong to expert e; out: device bf16 [E, M, H].  Each counted row goes
+ * through the activation quantisation, GEMM1, the activation with its
+ * re-quantisation and GEMM2 of its expert; out receives the bf16 GEMM2
+ * output in the same row.  Rows past a count are neither read nor written.
+ * 0 <= M and E * roundup(M, 128) <= the capacity moe_create sized for
+ * max_tokens * top_k routed rows (else MOE_ERR_UNSUPPORTED); M == 0 is a
+ * no-op.  A count outside [0, M] is clamped to that range and recorded as
+ * MOE_ERR_INVALID_ARG for moe_get_status.  Asynchronous on `stream`,
+ * allocates nothing.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED,
+ * MOE_ERR_NO_WEIGHTS, MOE_ERR_CUDA.                                        */
+moe_status moe_forward_batched(moe_layer *layer, const void *hidden,
+                               const int32_t *counts, int M, void *out,
+                               void *stream);
 
 /* Same as moe_forward with HOST buffers: copies hidden [T,H] bf16 and
  * router_logits [T,E] f32 to the device, runs the layer and copies out
@@ -150,9 +178,10 @@ moe_status moe_debug_intermediates(moe_layer *layer, float *h, float *y,
                                    void *stream);
 
 /* Device-side error word of the handle: synchronises the device, returns
- * MOE_ERR_DEVICE_TIMEOUT if any kernel gave up a bounded wait since the
- * last call (and clears it), MOE_ERR_CUDA on a sticky CUDA error, else
- * MOE_OK.                                                                  */
+ * the first error a kernel recorded since the last call (and clears it):
+ * MOE_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait,
+ * MOE_ERR_INVALID_ARG if moe_forward_batched met a count outside [0, M];
+ * MOE_ERR_CUDA on a sticky CUDA error; else MOE_OK.                        */
 moe_status moe_get_status(moe_layer *layer);
 
 /* Per-kernel timing (profiling).  While on, every moe_forward records a CUDA

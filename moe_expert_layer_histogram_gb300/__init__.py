@@ -16,6 +16,7 @@ from . import _build
 LIB_PATH = _build.LIB
 
 MOE_FMT = {"bf16": 0, "mxfp8": 1, "nvfp4": 2}
+MOE_ACT = {"swiglu": 0, "relu2": 1}
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_NO_WEIGHTS", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_OOM",
@@ -26,7 +27,7 @@ class MoEConfig(ctypes.Structure):
     _fields_ = [("max_tokens", ctypes.c_int), ("hidden", ctypes.c_int),
                 ("inter", ctypes.c_int), ("num_experts", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("format", ctypes.c_int),
-                ("clamp_limit", ctypes.c_float)]
+                ("clamp_limit", ctypes.c_float), ("activation", ctypes.c_int)]
 
 
 class MoEError(RuntimeError):
@@ -36,7 +37,8 @@ class MoEError(RuntimeError):
                                            moe_status_string(code)))
 
 
-EXPORTS = ("moe_create", "moe_prepare_weights", "moe_forward", "moe_forward_host",
+EXPORTS = ("moe_create", "moe_prepare_weights", "moe_forward", "moe_forward_batched",
+           "moe_forward_host",
            "moe_debug_routing", "moe_debug_act_quant", "moe_debug_intermediates",
            "moe_get_status", "moe_timing_start", "moe_timing_stop", "moe_last_launch_count",
            "moe_route_permute_static", "moe_measure_mma_rate", "moe_status_string",
@@ -58,6 +60,7 @@ def lib():
     L.moe_prepare_weights.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_forward.argtypes = [vp, vp, vp, vp, ci, vp]
     L.moe_forward_host.argtypes = [vp, vp, vp, vp, ci, vp]
+    L.moe_forward_batched.argtypes = [vp, vp, vp, ci, vp, vp]
     L.moe_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp]
     L.moe_debug_act_quant.argtypes = [vp, vp, vp, vp]
     L.moe_debug_intermediates.argtypes = [vp, vp, vp, vp]
@@ -96,9 +99,11 @@ def moe_status_string(code):
     return lib().moe_status_string(int(code)).decode()
 
 
-def moe_create(max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit=0.0):
+def moe_create(max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit=0.0,
+               activation="swiglu"):
     cfg = MoEConfig(int(max_tokens), int(hidden), int(inter), int(num_experts), int(top_k),
-                    MOE_FMT[fmt] if isinstance(fmt, str) else int(fmt), float(clamp_limit or 0.0))
+                    MOE_FMT[fmt] if isinstance(fmt, str) else int(fmt), float(clamp_limit or 0.0),
+                    MOE_ACT[activation] if isinstance(activation, str) else int(activation))
     h = ctypes.c_void_p()
     _check(lib().moe_create(ctypes.byref(cfg), ctypes.byref(h)), "moe_create")
     return h.value
@@ -113,6 +118,11 @@ def moe_prepare_weights(handle, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, stream=No
 def moe_forward(handle, hidden, router_logits, out, T, stream=None):
     _check(lib().moe_forward(handle, _ptr(hidden), _ptr(router_logits), _ptr(out), int(T), stream),
            "moe_forward")
+
+
+def moe_forward_batched(handle, hidden, counts, M, out, stream=None):
+    _check(lib().moe_forward_batched(handle, _ptr(hidden), _ptr(counts), int(M), _ptr(out),
+                                     stream), "moe_forward_batched")
 
 
 def moe_forward_host(handle, hidden_host, router_logits_host, out_host, T, stream=None):
@@ -188,13 +198,15 @@ class MoELayer:
     """One layer on the current CUDA device; tensors are torch CUDA tensors,
     work goes on torch's current stream."""
 
-    def __init__(self, max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit=0.0):
+    def __init__(self, max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit=0.0,
+                 activation="swiglu"):
         import torch
         self.torch = torch
         self.H, self.I, self.E, self.K = hidden, inter, num_experts, top_k
         self.fmt = fmt
         self.max_tokens = max_tokens
-        self.handle = moe_create(max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit)
+        self.handle = moe_create(max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit,
+                                 activation)
         self.T = 0
 
     def _stream(self):
@@ -215,6 +227,18 @@ class MoELayer:
             out = torch.empty_like(hidden)
         moe_forward(self.handle, hidden, router_logits, out, T, self._stream())
         self.T = T
+        return out
+
+    def forward_batched(self, hidden, counts, out=None):
+        """hidden bf16 [E, M, H], counts int32 [E] (device) -> out bf16
+        [E, M, H] (rows past a count are left as they are)."""
+        torch = self.torch
+        E, M, H = hidden.shape
+        assert E == self.E and H == self.H and hidden.dtype == torch.bfloat16
+        assert hidden.is_cuda and hidden.is_contiguous() and counts.dtype == torch.int32
+        if out is None:
+            out = torch.zeros_like(hidden)
+        moe_forward_batched(self.handle, hidden, counts, M, out, self._stream())
         return out
 
     def routing(self):

@@ -34,6 +34,8 @@ struct moe_layer {
   int xb = 0, hb = 0;                // bytes per row: GEMM1 / GEMM2 input
   int x_tiles_k = 0, h_tiles_k = 0;  // 128x4 scale tiles per 128-row block
   float clamp = INFINITY;
+  int act = MOE_ACT_SWIGLU;
+  int w13_rows = 0;                  // 2I (SwiGLU: gate and up) or I (ReLU^2)
   std::vector<void*> allocs;
   int32_t *ids = nullptr, *blockhist = nullptr, *prefix = nullptr;
   int32_t *offsets = nullptr, *pad_off = nullptr, *chunk_off = nullptr, *counts = nullptr;
@@ -46,6 +48,7 @@ struct moe_layer {
   float* l_in = nullptr;
   GemmMaps maps1{}, maps2{};
   int pair_scale_copies = 1;
+  int l2_prefetch = 0;               // GEMM stages prefetched into L2 ahead of the ring
   bool weights_ready = false;
   int last_T = 0, last_launches = 0;
   std::vector<cudaEvent_t> tev;  // per-kernel timing events, 7 per forward
@@ -119,9 +122,69 @@ void free_all(moe_layer* L) {
 // GEMM2 +35 %), so it is used up to this many tokens.
 constexpr int kPairCopyMaxTokens = 1024;
 
+// GEMM stages whose operands the producer prefetches into L2 ahead of its
+// shared-memory ring.
+constexpr int kDefaultL2Prefetch = 8;
+
 int64_t max_chunks(const moe_layer* L, int T) {
   const int64_t R = static_cast<int64_t>(T) * L->K;
   return std::min<int64_t>(L->E, R) + R / kRowBlock;
+}
+
+// GEMM1 (+ the activation and re-quantisation) over the padded
+// activation rows of the current tables.  max_rows bounds the rows of any
+// expert (selects the activation tile height).
+cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, cudaStream_t s) {
+  GemmArgs a{};
+  a.chunk_off = L->chunk_off;
+  a.pad_off = L->pad_off;
+  a.counts = L->counts;
+  a.E = L->E;
+  a.n_tiles = L->w13_rows / 128;
+  a.num_kb = L->xb / 128;
+  a.sfa = L->xsf;
+  a.sfa_tiles_k = L->x_tiles_k;
+  a.b_tiles = L->w13t;
+  a.b_tile_bytes = weight_tile_bytes(L->fmt);
+  a.out = L->hq;
+  a.out_ld = L->hb;
+  a.out_sf = L->hsf;
+  a.out_sf_tiles_k = L->h_tiles_k;
+  a.clamp = L->clamp;
+  a.pair_scale_copies = pair;
+  a.l2_prefetch = L->l2_prefetch;
+  a.out_rows_per_expert = 0;
+  a.status = L->status;
+  const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
+  return launch_gemm(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a, grid, max_rows, s);
+}
+
+// GEMM2 into `out` (bf16, H per row): padded rows (rows_per_expert 0) or
+// rows e*rows_per_expert + i (batched format).
+cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, void* out,
+                      int rows_per_expert, cudaStream_t s) {
+  GemmArgs a{};
+  a.chunk_off = L->chunk_off;
+  a.pad_off = L->pad_off;
+  a.counts = L->counts;
+  a.E = L->E;
+  a.n_tiles = L->H / 128;
+  a.num_kb = L->hb / 128;
+  a.sfa = L->hsf;
+  a.sfa_tiles_k = L->h_tiles_k;
+  a.b_tiles = L->w2t;
+  a.b_tile_bytes = weight_tile_bytes(L->fmt);
+  a.out = static_cast<uint8_t*>(out);
+  a.out_ld = static_cast<int64_t>(L->H) * 2;
+  a.out_sf = nullptr;
+  a.out_sf_tiles_k = 0;
+  a.clamp = INFINITY;
+  a.pair_scale_copies = pair;
+  a.l2_prefetch = L->l2_prefetch;
+  a.out_rows_per_expert = rows_per_expert;
+  a.status = L->status;
+  const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
+  return launch_gemm(L->fmt, 2, L->maps2, a, grid, max_rows, s);
 }
 
 }  // namespace
@@ -150,6 +213,9 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   if (c.max_tokens < 1 || c.hidden < 1 || c.inter < 1 || c.num_experts < 1 || c.top_k < 1)
     return MOE_ERR_INVALID_ARG;
   if (c.format < MOE_FMT_BF16 || c.format > MOE_FMT_NVFP4) return MOE_ERR_INVALID_ARG;
+  if (c.activation != MOE_ACT_SWIGLU && c.activation != MOE_ACT_RELU2) return MOE_ERR_INVALID_ARG;
+  if (c.activation == MOE_ACT_RELU2 && c.clamp_limit > 0.0f && std::isfinite(c.clamp_limit))
+    return MOE_ERR_UNSUPPORTED;
   const int kq = c.format == MOE_FMT_NVFP4 ? 256 : 128;
   if (c.hidden % kq || c.inter % kq || c.num_experts > kMaxExperts || c.top_k > kMaxTopK ||
       c.top_k > c.num_experts)
@@ -197,8 +263,15 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   L->Rpad = Rpad;
   L->NBmax = (c.max_tokens + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
   L->clamp = (c.clamp_limit > 0.0f && std::isfinite(c.clamp_limit)) ? c.clamp_limit : INFINITY;
+  L->act = c.activation;
+  L->w13_rows = c.activation == MOE_ACT_RELU2 ? c.inter : 2 * c.inter;
   // MOE_PAIR_SCALE_COPIES=0 turns the decode-sized scale-copy path off.
   L->pair_scale_copies = !(pv && pv[0] == '0');
+  // MOE_L2_PREFETCH=n: prefetch the operands of the GEMM stage n ahead into L2.
+  {
+    const char* v = std::getenv("MOE_L2_PREFETCH");
+    L->l2_prefetch = v ? std::max(0, std::min(64, std::atoi(v))) : kDefaultL2Prefetch;
+  }
   const int H = L->H, I = L->I, E = L->E;
   if (L->fmt == MOE_FMT_NVFP4) {
     L->xb = H / 2; L->hb = I / 2; L->x_tiles_k = H / 64; L->h_tiles_k = I / 64;
@@ -220,7 +293,7 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
             A.get(&L->hq, static_cast<size_t>(Rpad) * L->hb) &&
             A.get(&L->hsf, rblocks * L->h_tiles_k * 512) &&
             A.get(&L->y, static_cast<size_t>(Rpad) * H * 2) &&
-            A.get(&L->w13t, static_cast<size_t>(E) * (2 * I / 128) * (L->xb / 128) *
+            A.get(&L->w13t, static_cast<size_t>(E) * (L->w13_rows / 128) * (L->xb / 128) *
                                 weight_tile_bytes(L->fmt)) &&
             A.get(&L->w2t, static_cast<size_t>(E) * (H / 128) * (L->hb / 128) *
                                weight_tile_bytes(L->fmt)) &&
@@ -263,7 +336,8 @@ moe_status moe_prepare_weights(moe_layer* L, const void* w13, const void* w13_sf
   const int E = L->E, H = L->H, I = L->I;
   cudaError_t e = launch_tile_weights(L->fmt, static_cast<const uint8_t*>(w13),
                                       static_cast<const uint8_t*>(w13_sf), w13_gs, L->w13t, E,
-                                      2 * I, L->xb, L->x_tiles_k * 4, I, s);
+                                      L->w13_rows, L->xb, L->x_tiles_k * 4,
+                                      L->act == MOE_ACT_RELU2 ? 0 : I, s);
   if (e == cudaSuccess)
     e = launch_tile_weights(L->fmt, static_cast<const uint8_t*>(w2),
                             static_cast<const uint8_t*>(w2_sf), w2_gs, L->w2t, E, H, L->hb,
@@ -284,7 +358,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   if (!hidden || !logits || !out) return MOE_ERR_INVALID_ARG;
   if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int E = L->E, K = L->K, H = L->H, I = L->I;
+  const int E = L->E, K = L->K, H = L->H;
   const int NB = (T + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
   cudaEvent_t* ev = nullptr;
   if (L->timing_rec < L->timing_max) ev = &L->tev[static_cast<size_t>(L->timing_rec++) * 7];
@@ -301,57 +375,39 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
                              L->pad_off, L->chunk_off, L->perm, L->inv, L->xq, L->xsf, s);
   mark(3);
   const int64_t chunks = max_chunks(L, T);
-  if (e == cudaSuccess) {
-    GemmArgs a{};
-    a.chunk_off = L->chunk_off;
-    a.pad_off = L->pad_off;
-    a.counts = L->counts;
-    a.E = E;
-    a.n_tiles = I / 64;
-    a.num_kb = L->xb / 128;
-    a.sfa = L->xsf;
-    a.sfa_tiles_k = L->x_tiles_k;
-    a.b_tiles = L->w13t;
-    a.b_tile_bytes = weight_tile_bytes(L->fmt);
-    a.out = L->hq;
-    a.out_ld = L->hb;
-    a.out_sf = L->hsf;
-    a.out_sf_tiles_k = L->h_tiles_k;
-    a.clamp = L->clamp;
-    a.pair_scale_copies = L->pair_scale_copies && T <= kPairCopyMaxTokens;
-    a.status = L->status;
-    const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
-    e = launch_gemm(L->fmt, 1, L->maps1, a, grid, T, s);
-  }
+  const int pair = L->pair_scale_copies && T <= kPairCopyMaxTokens;
+  if (e == cudaSuccess) e = run_gemm1(L, chunks, T, pair, s);
   mark(4);
-  if (e == cudaSuccess) {
-    GemmArgs a{};
-    a.chunk_off = L->chunk_off;
-    a.pad_off = L->pad_off;
-    a.counts = L->counts;
-    a.E = E;
-    a.n_tiles = H / 128;
-    a.num_kb = L->hb / 128;
-    a.sfa = L->hsf;
-    a.sfa_tiles_k = L->h_tiles_k;
-    a.b_tiles = L->w2t;
-    a.b_tile_bytes = weight_tile_bytes(L->fmt);
-    a.out = L->y;
-    a.out_ld = static_cast<int64_t>(H) * 2;
-    a.out_sf = nullptr;
-    a.out_sf_tiles_k = 0;
-    a.clamp = INFINITY;
-    a.pair_scale_copies = L->pair_scale_copies && T <= kPairCopyMaxTokens;
-    a.status = L->status;
-    const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
-    e = launch_gemm(L->fmt, 2, L->maps2, a, grid, T, s);
-  }
+  if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, L->y, 0, s);
   mark(5);
   if (e == cudaSuccess) e = launch_combine(L->y, L->inv, L->w, T, K, H, out, s);
   mark(6);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   L->last_T = T;
   L->last_launches = 6;
+  return MOE_OK;
+}
+
+moe_status moe_forward_batched(moe_layer* L, const void* hidden, const int32_t* counts, int M,
+                               void* out, void* stream) {
+  if (!L || M < 0) return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  if (!hidden || !counts || !out) return MOE_ERR_INVALID_ARG;
+  if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
+  const int64_t mpad = (static_cast<int64_t>(M) + kRowBlock - 1) / kRowBlock * kRowBlock;
+  if (mpad * L->E > L->Rpad) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t chunks = mpad / kRowBlock * L->E;
+  // every chunk holds at most 32 rows when M <= 32: the lanes-0-31 scale copies apply
+  const int pair = L->pair_scale_copies && M <= 32;
+  cudaError_t e = launch_batched_quant(L->fmt, hidden, counts, M, L->E, L->H, L->counts,
+                                       L->offsets, L->pad_off, L->chunk_off, L->xq, L->xsf,
+                                       L->status, s);
+  if (e == cudaSuccess) e = run_gemm1(L, chunks, M, pair, s);
+  if (e == cudaSuccess) e = run_gemm2(L, chunks, M, pair, out, M, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  L->last_T = 0;
+  L->last_launches = 3;
   return MOE_OK;
 }
 
@@ -419,7 +475,7 @@ moe_status moe_get_status(moe_layer* L) {
     return MOE_ERR_CUDA;
   if (v != 0) {
     cudaMemset(L->status, 0, sizeof(int));
-    return MOE_ERR_DEVICE_TIMEOUT;
+    return v == kStatusBadCount ? MOE_ERR_INVALID_ARG : MOE_ERR_DEVICE_TIMEOUT;
   }
   return MOE_OK;
 }

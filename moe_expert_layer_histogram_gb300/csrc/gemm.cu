@@ -6,8 +6,8 @@
 // with A and W in BF16, MXFP8 (e4m3, e8m0 per 32) or NVFP4 (e2m1, e4m3 per
 // 16, global scale folded in); the block-scaled MMA applies both operands'
 // scales.  GEMM1's epilogue applies SwiGLU with the optional gate/up clamp
-// and re-quantises the result into GEMM2's input format; GEMM2's epilogue
-// stores bf16.  (The two expert GEMMs with SwiGLU between them: PR #40082
+// (or the non-gated squared ReLU) and re-quantises the result into GEMM2's
+// input format; GEMM2's epilogue stores bf16.  (The two expert GEMMs with SwiGLU between them: PR #40082
 // report, sec. 实现拆解 item 1.)
 //
 // Structure: one persistent CTA per SM walks the device-built work list
@@ -220,6 +220,93 @@ __device__ __forceinline__ void epilogue_gemm1(uint32_t taddr, bool store, int64
   }
 }
 
+// GEMM1 with the non-gated squared ReLU: thread = accumulator row; the 128
+// columns are intermediate features 128*n_tile + j, h = max(x, 0)^2 (one
+// correctly rounded fp32 product), then the same re-quantisation per 16-
+// (NVFP4) or 32- (MXFP8) block, or a bf16 round.
+__device__ __forceinline__ float relu_sq(float x) {
+  x = fmaxf(x, 0.0f);
+  return __fmul_rn(x, x);
+}
+
+template <int FMT>
+__device__ __forceinline__ void epilogue_relu2(uint32_t taddr, bool store, int64_t prow,
+                                               int n_tile, const GemmArgs& a) {
+  if constexpr (FMT == kFmtNVFP4) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t packed[8];
+      uint32_t sf4 = 0;
+#pragma unroll
+      for (int jb = 0; jb < 4; ++jb) {
+        uint32_t v[16];
+        tmem_ld16(taddr + half * 64 + jb * 16, v);
+        tmem_ld_wait();
+        reg_fence16(v);
+        float h[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) h[i] = relu_sq(lane_value(v[i], store));
+        uint32_t c[2];
+        uint8_t sf;
+        quant_nvfp4_16(h, c, sf);
+        packed[2 * jb] = c[0];
+        packed[2 * jb + 1] = c[1];
+        sf4 |= static_cast<uint32_t>(sf) << (8 * jb);
+      }
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + half * 32);
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        *reinterpret_cast<uint32_t*>(
+            a.out_sf + sf_tile_offset(prow, n_tile * 8 + half * 4, a.out_sf_tiles_k)) = sf4;
+      }
+    }
+  } else if constexpr (FMT == kFmtMXFP8) {
+#pragma unroll
+    for (int jb = 0; jb < 4; ++jb) {
+      float h[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[16];
+        tmem_ld16(taddr + jb * 32 + half * 16, v);
+        tmem_ld_wait();
+        reg_fence16(v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) h[half * 16 + i] = relu_sq(lane_value(v[i], store));
+      }
+      uint32_t c[8];
+      uint8_t sf;
+      quant_mxfp8_32(h, c, sf);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 128 + jb * 32);
+        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+        a.out_sf[sf_tile_offset(prow, n_tile * 4 + jb, a.out_sf_tiles_k)] = sf;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int jb = 0; jb < 8; ++jb) {
+      uint32_t v[16];
+      tmem_ld16(taddr + jb * 16, v);
+      tmem_ld_wait();
+      reg_fence16(v);
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(relu_sq(lane_value(v[2 * i], store)),
+                                                       relu_sq(lane_value(v[2 * i + 1], store)));
+        o[i] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + (n_tile * 128 + jb * 16) * 2);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+  }
+}
+
 // GEMM2: 128 output features per row, stored as bf16.
 __device__ __forceinline__ void epilogue_gemm2(uint32_t taddr, bool store, int64_t prow,
                                                int n_tile, const GemmArgs& a) {
@@ -300,7 +387,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t policy = l2_policy_evict_first();
+      // A weight tile read by one chunk only (decode) is dead after this
+      // read; one read by several chunks of its expert stays in L2 for them.
+      const uint64_t pol_once = l2_policy_evict_first(), pol_shared = l2_policy_evict_normal();
+      const int pf = args.l2_prefetch;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -317,7 +407,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint8_t* btile =
             args.b_tiles + (static_cast<int64_t>(it.e) * args.n_tiles + it.n_tile) * args.num_kb *
                                args.b_tile_bytes;
+        const uint64_t policy =
+            tab.chunk_off[it.e + 1] - tab.chunk_off[it.e] > 1 ? pol_shared : pol_once;
+        // Warm L2 with the operands of the stages `pf` ahead of the ring:
+        // the copies then find them in L2 instead of waiting on HBM (many
+        // CTAs read the same weight tile at about the same time).
+        for (int kb = 0; kb < pf && kb < args.num_kb; ++kb) {
+          prefetch_l2(btile + static_cast<int64_t>(kb) * args.b_tile_bytes, args.b_tile_bytes);
+          prefetch_l2_tile(&maps.a[amap], kb * 128, it.prow0);
+        }
         for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (pf && kb + pf < args.num_kb) {
+            prefetch_l2(btile + static_cast<int64_t>(kb + pf) * args.b_tile_bytes,
+                        args.b_tile_bytes);
+            prefetch_l2_tile(&maps.a[amap], (kb + pf) * 128, it.prow0);
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -459,7 +563,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols;
         const int64_t prow = it.prow0 + r;
         if constexpr (EPI == 1) epilogue_gemm1<FMT>(taddr, r < it.rows, prow, it.n_tile, args);
-        else epilogue_gemm2(taddr, r < it.rows, prow, it.n_tile, args);
+        else if constexpr (EPI == 3) epilogue_relu2<FMT>(taddr, r < it.rows, prow, it.n_tile, args);
+        else {
+          // batched format: expert e's rows go to rows e*M.. of the output
+          const int64_t orow =
+              args.out_rows_per_expert
+                  ? static_cast<int64_t>(it.e) * args.out_rows_per_expert +
+                        (it.prow0 - tab.pad_off[it.e]) + r
+                  : prow;
+          epilogue_gemm2(taddr, r < it.rows, orow, it.n_tile, args);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -484,6 +597,9 @@ cudaError_t prepare_m() {
   cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<FMT, 1, MROWS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem_bytes<FMT, MROWS>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(moe_gemm_kernel<FMT, 3, MROWS>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<FMT, MROWS>());
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(moe_gemm_kernel<FMT, 2, MROWS>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<FMT, MROWS>());
@@ -516,13 +632,16 @@ cudaError_t gemm_prepare(int fmt) {
 cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& args, int grid,
                         int max_rows, cudaStream_t s) {
   if (fmt == kFmtBF16)
-    return epi == 1 ? launch_fmt<kFmtBF16, 1>(maps, args, grid, max_rows, s)
-                    : launch_fmt<kFmtBF16, 2>(maps, args, grid, max_rows, s);
+    return epi == 1   ? launch_fmt<kFmtBF16, 1>(maps, args, grid, max_rows, s)
+           : epi == 3 ? launch_fmt<kFmtBF16, 3>(maps, args, grid, max_rows, s)
+                      : launch_fmt<kFmtBF16, 2>(maps, args, grid, max_rows, s);
   if (fmt == kFmtMXFP8)
-    return epi == 1 ? launch_fmt<kFmtMXFP8, 1>(maps, args, grid, max_rows, s)
-                    : launch_fmt<kFmtMXFP8, 2>(maps, args, grid, max_rows, s);
-  return epi == 1 ? launch_fmt<kFmtNVFP4, 1>(maps, args, grid, max_rows, s)
-                  : launch_fmt<kFmtNVFP4, 2>(maps, args, grid, max_rows, s);
+    return epi == 1   ? launch_fmt<kFmtMXFP8, 1>(maps, args, grid, max_rows, s)
+           : epi == 3 ? launch_fmt<kFmtMXFP8, 3>(maps, args, grid, max_rows, s)
+                      : launch_fmt<kFmtMXFP8, 2>(maps, args, grid, max_rows, s);
+  return epi == 1   ? launch_fmt<kFmtNVFP4, 1>(maps, args, grid, max_rows, s)
+         : epi == 3 ? launch_fmt<kFmtNVFP4, 3>(maps, args, grid, max_rows, s)
+                    : launch_fmt<kFmtNVFP4, 2>(maps, args, grid, max_rows, s);
 }
 
 }  // namespace moe

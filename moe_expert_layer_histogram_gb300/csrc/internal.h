@@ -16,6 +16,17 @@ constexpr int kTokensPerRouteBlock = 8;   // tokens per routing/scatter block (w
 constexpr int kRowBlock = 128;            // expert segments padded to this
 constexpr int kGemmThreads = 192;         // producer, MMA, 4 epilogue warps
 
+// Device status word codes (read back by moe_get_status).
+constexpr int kStatusBadCount = 1;  // MOE_ERR_INVALID_ARG: a batched count outside [0, M]
+constexpr int kStatusTimeout = 6;   // MOE_ERR_DEVICE_TIMEOUT: a bounded wait gave up
+
+#ifdef __CUDACC__
+// First error wins.
+__device__ __forceinline__ void report_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+#endif
+
 // Per-launch arguments of the grouped GEMMs.  Work items are (expert,
 // output tile of 128 columns of the weight rows, 128-row token chunk),
 // expert-major, then output tile, then chunk.
@@ -36,6 +47,9 @@ struct GemmArgs {
   int out_sf_tiles_k;
   float clamp;               // +inf: no clamp
   int pair_scale_copies;     // 1: chunks of <= 32 rows copy scales to lanes 0-31 only
+  int l2_prefetch;           // stages ahead whose operands are prefetched into L2 (0: off)
+  int out_rows_per_expert;   // 0: output row = padded row; M > 0 (batched format):
+                             // output row = e * M + row within the expert
   int* status;
 };
 
@@ -88,6 +102,8 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 cudaError_t gemm_prepare(int fmt);  // raise the dynamic shared-memory limit
 // max_rows: upper bound on the rows of any expert in this launch (<= T);
 // selects the activation-tile height of the shared-memory stages.
+// epi: 1 = GEMM1 + SwiGLU, 3 = GEMM1 + ReLU^2 (both re-quantise into the
+// GEMM2 input format), 2 = GEMM2 (bf16 out).
 cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& args, int grid,
                         int max_rows, cudaStream_t s);
 
@@ -103,6 +119,12 @@ cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int 
                                  uint8_t* xsf, cudaStream_t s);
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int K, int H,
                            void* out, cudaStream_t s);
+// Batched-expert format: per-expert tables from the counts and the GEMM1
+// input rows of hidden [E, M, H].
+cudaError_t launch_batched_quant(int fmt, const void* hidden, const int32_t* counts_in, int M,
+                                 int E, int H, int32_t* counts, int32_t* offsets,
+                                 int32_t* pad_off, int32_t* chunk_off, uint8_t* xq, uint8_t* xsf,
+                                 int* status, cudaStream_t s);
 
 // Weight preparation.
 cudaError_t launch_tile_weights(int fmt, const uint8_t* codes, const uint8_t* sf, const float* gs,

@@ -11,7 +11,6 @@ namespace moe {
 // A wait that does not finish within this many nanoseconds gives up: the
 // kernel records MOE_ERR_DEVICE_TIMEOUT and returns instead of hanging.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
-constexpr int kStatusTimeout = 6;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -23,9 +22,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ void report_status(int* status, int code) {
-  if (status) atomicCAS(status, 0, code);
-}
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -122,6 +118,26 @@ __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint3
       " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bring global memory into L2 ahead of the copy that will read it (no
+// completion tracking; a prefetch only warms the cache).  Address 16-byte
+// aligned, size a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2_tile(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {

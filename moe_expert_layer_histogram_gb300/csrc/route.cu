@@ -25,6 +25,73 @@ namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
+// ---------------------------------------------------------------- row quantisation
+// bf16 -> fp32 for N consecutive elements (N a multiple of 8, 16-byte aligned).
+template <int N>
+__device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float (&f)[N]) {
+  const uint4* src = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int h = 0; h < N / 8; ++h) {
+    const uint4 u = src[h];
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+      f[8 * h + 2 * q] = v.x;
+      f[8 * h + 2 * q + 1] = v.y;
+    }
+  }
+}
+
+// One warp writes the GEMM1 input of one token row x [H] into the padded
+// rows prows[0..n): BF16 copied, MXFP8 / NVFP4 quantised per block (lane l
+// takes blocks l, l+32, ...), codes row-major and scales in the MMA's
+// 128-row scale tiles.
+template <int FMT>
+__device__ __forceinline__ void quant_row_to_rows(const __nv_bfloat16* __restrict__ x, int H,
+                                                  const int* prows, int n,
+                                                  uint8_t* __restrict__ xq,
+                                                  uint8_t* __restrict__ xsf, int lane) {
+  if constexpr (FMT == kFmtBF16) {
+    const uint4* src = reinterpret_cast<const uint4*>(x);
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 val = src[c];
+      for (int k = 0; k < n; ++k)
+        reinterpret_cast<uint4*>(xq + static_cast<int64_t>(prows[k]) * H * 2)[c] = val;
+    }
+  } else if constexpr (FMT == kFmtNVFP4) {
+    const int tiles_k = H / 64;
+    for (int blk = lane; blk < H / 16; blk += 32) {
+      float f[16];
+      load_bf16<16>(x + blk * 16, f);
+      uint32_t codes[2];
+      uint8_t sf;
+      quant_nvfp4_16(f, codes, sf);
+      for (int k = 0; k < n; ++k) {
+        const int64_t prow = prows[k];
+        *reinterpret_cast<uint2*>(xq + prow * (H / 2) + blk * 8) = make_uint2(codes[0], codes[1]);
+        xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
+      }
+    }
+  } else {
+    const int tiles_k = H / 128;
+    for (int blk = lane; blk < H / 32; blk += 32) {
+      float f[32];
+      load_bf16<32>(x + blk * 32, f);
+      uint32_t codes[8];
+      uint8_t sf;
+      quant_mxfp8_32(f, codes, sf);
+      for (int k = 0; k < n; ++k) {
+        const int64_t prow = prows[k];
+        uint4* dst = reinterpret_cast<uint4*>(xq + prow * H + blk * 32);
+        dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- routing
 // One warp per token, 8 tokens per block.  Lane l holds logits l, l+32, ...;
 // K rounds of a warp arg-max in the total order (value descending, index
@@ -232,68 +299,72 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
 
   // 3. GEMM1 input rows
   if (warp >= ntok) return;
-  const __nv_bfloat16* x = hidden + static_cast<int64_t>(tok0 + warp) * H;
-  const int* prows = s_prow + warp * K;
-  if constexpr (FMT == kFmtBF16) {
-    const uint4* src = reinterpret_cast<const uint4*>(x);
-    for (int c = lane; c < H / 8; c += 32) {
-      const uint4 val = src[c];
-      for (int k = 0; k < K; ++k)
-        reinterpret_cast<uint4*>(xq + static_cast<int64_t>(prows[k]) * H * 2)[c] = val;
+  quant_row_to_rows<FMT>(hidden + static_cast<int64_t>(tok0 + warp) * H, H, s_prow + warp * K, K,
+                         xq, xsf, lane);
+}
+
+// ---------------------------------------------------------------- batched format
+// Batched-expert input [E, M, H] with per-expert counts: block (x, e)
+// writes the GEMM1 input of rows 8x..8x+7 of expert e (one warp each) into
+// that expert's 128-row-padded segment.  Every block scans the counts over
+// the experts itself (a block scan, E <= 512) for its segment base; block
+// (0, 0) also stores the tables the GEMMs read.  A count outside [0, M] is
+// clamped and reported through the status word.
+template <int FMT>
+__global__ void __launch_bounds__(256) batched_quant_kernel(
+    const __nv_bfloat16* __restrict__ hidden, const int32_t* __restrict__ counts_in, int M, int E,
+    int H, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ pad_off, int32_t* __restrict__ chunk_off, uint8_t* __restrict__ xq,
+    uint8_t* __restrict__ xsf, int* status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ int wsum[8];
+  __shared__ int s_base, s_cnt;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.y;
+  const bool first = blockIdx.x == 0 && blockIdx.y == 0;
+  const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
+  int c0 = e0 < E ? counts_in[e0] : 0, c1 = e1 < E ? counts_in[e1] : 0;
+  if (first && (c0 < 0 || c0 > M || c1 < 0 || c1 > M)) report_status(status, kStatusBadCount);
+  c0 = min(max(c0, 0), M);
+  c1 = min(max(c1, 0), M);
+  const int p0 = (c0 + kRowBlock - 1) / kRowBlock, p1 = (c1 + kRowBlock - 1) / kRowBlock;
+  const int xo = block_scan_pair(c0 + c1, wsum);
+  const int xp = block_scan_pair((p0 + p1) * kRowBlock, wsum);
+  const int xc = block_scan_pair(p0 + p1, wsum);
+  if (e0 == e) {
+    s_base = xp;
+    s_cnt = c0;
+  }
+  if (e1 == e) {
+    s_base = xp + p0 * kRowBlock;
+    s_cnt = c1;
+  }
+  if (first) {
+    if (e0 < E) {
+      counts[e0] = c0;
+      offsets[e0] = xo;
+      pad_off[e0] = xp;
+      chunk_off[e0] = xc;
     }
-  } else if constexpr (FMT == kFmtNVFP4) {
-    const int tiles_k = H / 64;
-    for (int blk = lane; blk < H / 16; blk += 32) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + blk * 16);
-      float f[16];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 u = src[h];
-        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
-          f[8 * h + 2 * q] = p.x;
-          f[8 * h + 2 * q + 1] = p.y;
-        }
-      }
-      uint32_t codes[2];
-      uint8_t sf;
-      quant_nvfp4_16(f, codes, sf);
-      for (int k = 0; k < K; ++k) {
-        const int64_t prow = prows[k];
-        *reinterpret_cast<uint2*>(xq + prow * (H / 2) + blk * 8) = make_uint2(codes[0], codes[1]);
-        xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
-      }
+    if (e1 < E) {
+      counts[e1] = c1;
+      offsets[e1] = xo + c0;
+      pad_off[e1] = xp + p0 * kRowBlock;
+      chunk_off[e1] = xc + p0;
     }
-  } else {
-    const int tiles_k = H / 128;
-    for (int blk = lane; blk < H / 32; blk += 32) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + blk * 32);
-      float f[32];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const uint4 u = src[h];
-        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
-          f[8 * h + 2 * q] = p.x;
-          f[8 * h + 2 * q + 1] = p.y;
-        }
-      }
-      uint32_t codes[8];
-      uint8_t sf;
-      quant_mxfp8_32(f, codes, sf);
-      for (int k = 0; k < K; ++k) {
-        const int64_t prow = prows[k];
-        uint4* dst = reinterpret_cast<uint4*>(xq + prow * H + blk * 32);
-        dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-        dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-        xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
-      }
+    if (e0 == E - 1 || e1 == E - 1) {
+      offsets[E] = xo + c0 + c1;
+      pad_off[E] = xp + (p0 + p1) * kRowBlock;
+      chunk_off[E] = xc + p0 + p1;
     }
   }
+  __syncthreads();
+  const int r = blockIdx.x * kTokensPerRouteBlock + warp;
+  if (r >= s_cnt) return;
+  const int prow = s_base + r;
+  quant_row_to_rows<FMT>(hidden + (static_cast<int64_t>(e) * M + r) * H, H, &prow, 1, xq, xsf,
+                         lane);
 }
 
 // ---------------------------------------------------------------- combine
@@ -419,6 +490,19 @@ cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int 
                               : scatter_quant_kernel<kFmtNVFP4>;
   return launch_pdl(g_pdl_small, k, dim3(nb), dim3(256), 0, s, ids, T, E, K, hb, H, prefix,
                     counts, offsets, pad_off, chunk_off, perm, inv, xq, xsf);
+}
+
+cudaError_t launch_batched_quant(int fmt, const void* hidden, const int32_t* counts_in, int M,
+                                 int E, int H, int32_t* counts, int32_t* offsets,
+                                 int32_t* pad_off, int32_t* chunk_off, uint8_t* xq, uint8_t* xsf,
+                                 int* status, cudaStream_t s) {
+  const dim3 grid((M + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock, E);
+  const auto* hb = static_cast<const __nv_bfloat16*>(hidden);
+  auto k = fmt == kFmtBF16 ? batched_quant_kernel<kFmtBF16>
+           : fmt == kFmtMXFP8 ? batched_quant_kernel<kFmtMXFP8>
+                              : batched_quant_kernel<kFmtNVFP4>;
+  return launch_pdl(g_pdl_small, k, grid, dim3(256), 0, s, hb, counts_in, M, E, H, counts,
+                    offsets, pad_off, chunk_off, xq, xsf, status);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int K, int H,

@@ -215,3 +215,111 @@ def test_mma_rate_measurement():
     assert fp8 > 1.5 * bf16 and fp4 > 1.5 * fp8, (bf16, fp8, fp4)
     with_copies = moe_measure_mma_rate("nvfp4", 128, copy_scales=True, iters=4000)
     assert 0 < with_copies
+
+
+# ---- the non-gated ReLU^2 activation ---------------------------------------
+@pytest.mark.parametrize("name,over", [
+    ("bf16_small", dict(clamp=0.0, act="relu2")),
+    ("mxfp8_small", dict(act="relu2")),
+    ("nvfp4_small", dict(act="relu2")),
+    ("nvfp4_small", dict(T=200, E=3, K=2, act="relu2")),
+], ids=["bf16", "mxfp8", "nvfp4", "nvfp4-chunks"])
+def test_relu2_layer_matches_oracle(name, over):
+    s = workloads.spec(name, **over)
+    case = workloads.make_case(s, seed=3)
+    ref = run_oracle(s, case, intermediates=True)
+    layer = make_layer(s, weights=case["weights"])
+    out = run_gpu(layer, case["hidden"], case["logits"])
+    ids, w, off, perm = (t.cpu().numpy() for t in layer.routing())
+    assert np.array_equal(ids, ref["ids"]) and np.array_equal(perm, ref["perm"])
+    h, y = (t.cpu().numpy() for t in layer.intermediates())
+    assert rel_l2(h, ref["h"]) <= TOL[s["fmt"]], "GEMM2 input"
+    assert rel_l2(y, ref["y"]) <= TOL[s["fmt"]], "GEMM2 output"
+    assert rel_l2(out.float().cpu().numpy(), bf16_bits_to_f64(ref["out"])) <= TOL[s["fmt"]]
+    assert layer.status() == 0
+    layer.close()
+
+
+def test_relu2_with_clamp_is_unsupported():
+    from moe_expert_layer_histogram_gb300 import MoEError, moe_create
+    with pytest.raises(MoEError) as e:
+        moe_create(16, 256, 128, 8, 2, "bf16", 7.0, "relu2")
+    assert e.value.code == 2
+
+
+# ---- the batched-expert format ----------------------------------------------
+BATCHED = [
+    ("bf16_small", dict(clamp=0.5), 20),
+    ("mxfp8_small", dict(), 40),
+    ("nvfp4_small", dict(), 9),
+    ("nvfp4_small", dict(E=5), 300),          # several 128-row chunks per expert
+    ("nvfp4_small", dict(act="relu2"), 24),
+    ("mxfp8_small", dict(act="relu2", E=6), 130),
+]
+
+
+@pytest.mark.parametrize("name,over,M", BATCHED,
+                         ids=["%s-%d-M%d" % (b[0], i, b[2]) for i, b in enumerate(BATCHED)])
+def test_batched_format_matches_oracle(name, over, M):
+    import oracle
+    from tests.gpu_helpers import cfg_of
+    s = workloads.spec(name, **over)
+    case = workloads.make_case(s, T=1, seed=11)
+    hid, counts = workloads.draw_batched(s, M, seed=11)
+    npw = workloads.to_numpy_case(case)["weights"]
+    hb = hid.view(torch.int16).numpy().view("uint16")
+    ref = oracle.forward_batched(cfg_of(s), npw, hb, counts.numpy(), want_y=True)
+    layer = make_layer(s, max_tokens=max(1, (s["E"] * ((M + 127) // 128) * 128) // s["K"]),
+                       weights=case["weights"])
+    sentinel = torch.full((s["E"], M, s["H"]), 3.0, dtype=torch.bfloat16, device="cuda")
+    out = layer.forward_batched(hid.cuda(), counts.cuda(), out=sentinel)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    got = out.float().cpu().numpy()
+    cn = counts.numpy()
+    for e in range(s["E"]):
+        assert (got[e, cn[e]:] == 3.0).all(), "rows past the count were written"
+    mask = np.zeros(got.shape[:2], bool)
+    for e in range(s["E"]):
+        mask[e, :cn[e]] = True
+    assert rel_l2(got[mask], ref["y"][mask]) <= TOL[s["fmt"]]
+    # a row-by-row bound too: no single expert far off
+    for e in range(s["E"]):
+        if cn[e]:
+            assert rel_l2(got[e, :cn[e]], ref["y"][e, :cn[e]]) <= 2 * TOL[s["fmt"]], e
+    layer.close()
+
+
+def test_batched_counts_out_of_range_are_clamped_and_reported():
+    s = workloads.spec("nvfp4_small")
+    case = workloads.make_case(s, T=1, seed=2)
+    M = 16
+    hid, counts = workloads.draw_batched(s, M, seed=2)
+    layer = make_layer(s, max_tokens=s["E"] * 128 // s["K"], weights=case["weights"])
+    good = layer.forward_batched(hid.cuda(), counts.cuda()).clone()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    bad = counts.clone()
+    bad[1] = M + 5                                  # clamps to M (expert 1 is already full)
+    out = layer.forward_batched(hid.cuda(), bad.cuda())
+    assert layer.status() == 1                      # MOE_ERR_INVALID_ARG, then cleared
+    assert layer.status() == 0
+    assert torch.equal(out, good)
+    layer.close()
+
+
+def test_batched_capacity_and_arguments():
+    from moe_expert_layer_histogram_gb300 import MoEError, moe_forward_batched
+    s = workloads.spec("bf16_small")
+    case = workloads.make_case(s, T=1, seed=2)
+    layer = make_layer(s, max_tokens=8, weights=case["weights"])   # capacity: 8*4 rows + pads
+    hid = torch.zeros(s["E"], 600, s["H"], dtype=torch.bfloat16, device="cuda")
+    cnt = torch.zeros(s["E"], dtype=torch.int32, device="cuda")
+    with pytest.raises(MoEError) as e:
+        moe_forward_batched(layer.handle, hid, cnt, 600, hid)
+    assert e.value.code == 2
+    moe_forward_batched(layer.handle, hid, cnt, 0, hid)            # M == 0: no-op
+    with pytest.raises(MoEError) as e:
+        moe_forward_batched(layer.handle, hid, cnt, -1, hid)
+    assert e.value.code == 1
+    layer.close()
