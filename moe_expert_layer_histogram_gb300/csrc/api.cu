@@ -48,7 +48,7 @@ struct moe_layer {
   float* l_in = nullptr;
   GemmMaps maps1{}, maps2{};
   int pair_scale_copies = 1;
-  int l2_prefetch = 0;               // GEMM stages prefetched into L2 ahead of the ring
+  int wide_tiles = -1;               // 0 off, 1 always, -1 for prefill-sized launches
   bool weights_ready = false;
   int last_T = 0, last_launches = 0;
   std::vector<cudaEvent_t> tev;  // per-kernel timing events, 7 per forward
@@ -115,16 +115,18 @@ void free_all(moe_layer* L) {
   L->allocs.clear();
 }
 
+// Launches of more than kPairCopyMaxTokens tokens (mostly full 128-row
+// chunks) use GEMM items of two weight tiles (N = 256), which halves the
+// shared-memory traffic of the activation operand per FLOP.  BF16 and NVFP4
+// only: with the MXFP8 kind at N = 256 the second weight tile's scales are
+// not where the MMA reads them (results wrong), so MXFP8 keeps N = 128.
+//
 // Chunks of at most 32 rows can take their block scales in with half as
 // many TMEM copies (lanes 0-31 only).  Measured on GB300 this speeds up
 // decode-sized launches (every chunk that small) by 10-15 %, but slows a
 // prefill launch that mixes such chunks with full ones (Zipf-routed T=8192:
 // GEMM2 +35 %), so it is used up to this many tokens.
 constexpr int kPairCopyMaxTokens = 1024;
-
-// GEMM stages whose operands the producer prefetches into L2 ahead of its
-// shared-memory ring.
-constexpr int kDefaultL2Prefetch = 8;
 
 int64_t max_chunks(const moe_layer* L, int T) {
   const int64_t R = static_cast<int64_t>(T) * L->K;
@@ -134,13 +136,15 @@ int64_t max_chunks(const moe_layer* L, int T) {
 // GEMM1 (+ the activation and re-quantisation) over the padded
 // activation rows of the current tables.  max_rows bounds the rows of any
 // expert (selects the activation tile height).
-cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, cudaStream_t s) {
+cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide,
+                      cudaStream_t s) {
+  wide = wide && L->w13_rows % 256 == 0 && L->fmt != MOE_FMT_MXFP8;
   GemmArgs a{};
   a.chunk_off = L->chunk_off;
   a.pad_off = L->pad_off;
   a.counts = L->counts;
   a.E = L->E;
-  a.n_tiles = L->w13_rows / 128;
+  a.n_tiles = L->w13_rows / (wide ? 256 : 128);
   a.num_kb = L->xb / 128;
   a.sfa = L->xsf;
   a.sfa_tiles_k = L->x_tiles_k;
@@ -152,23 +156,24 @@ cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, cuda
   a.out_sf_tiles_k = L->h_tiles_k;
   a.clamp = L->clamp;
   a.pair_scale_copies = pair;
-  a.l2_prefetch = L->l2_prefetch;
   a.out_rows_per_expert = 0;
   a.status = L->status;
   const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
-  return launch_gemm(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a, grid, max_rows, s);
+  return launch_gemm(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a, grid, max_rows, wide,
+                     s);
 }
 
 // GEMM2 into `out` (bf16, H per row): padded rows (rows_per_expert 0) or
 // rows e*rows_per_expert + i (batched format).
-cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, void* out,
+cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide, void* out,
                       int rows_per_expert, cudaStream_t s) {
+  wide = wide && L->H % 256 == 0 && L->fmt != MOE_FMT_MXFP8;
   GemmArgs a{};
   a.chunk_off = L->chunk_off;
   a.pad_off = L->pad_off;
   a.counts = L->counts;
   a.E = L->E;
-  a.n_tiles = L->H / 128;
+  a.n_tiles = L->H / (wide ? 256 : 128);
   a.num_kb = L->hb / 128;
   a.sfa = L->hsf;
   a.sfa_tiles_k = L->h_tiles_k;
@@ -180,11 +185,10 @@ cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, void
   a.out_sf_tiles_k = 0;
   a.clamp = INFINITY;
   a.pair_scale_copies = pair;
-  a.l2_prefetch = L->l2_prefetch;
   a.out_rows_per_expert = rows_per_expert;
   a.status = L->status;
   const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
-  return launch_gemm(L->fmt, 2, L->maps2, a, grid, max_rows, s);
+  return launch_gemm(L->fmt, 2, L->maps2, a, grid, max_rows, wide, s);
 }
 
 }  // namespace
@@ -267,11 +271,9 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   L->w13_rows = c.activation == MOE_ACT_RELU2 ? c.inter : 2 * c.inter;
   // MOE_PAIR_SCALE_COPIES=0 turns the decode-sized scale-copy path off.
   L->pair_scale_copies = !(pv && pv[0] == '0');
-  // MOE_L2_PREFETCH=n: prefetch the operands of the GEMM stage n ahead into L2.
-  {
-    const char* v = std::getenv("MOE_L2_PREFETCH");
-    L->l2_prefetch = v ? std::max(0, std::min(64, std::atoi(v))) : kDefaultL2Prefetch;
-  }
+  // MOE_WIDE_TILES=0|1: never / always use the N = 256 GEMM items (default:
+  // for launches of more than kPairCopyMaxTokens tokens).
+  if (const char* wv = std::getenv("MOE_WIDE_TILES")) L->wide_tiles = wv[0] == '0' ? 0 : 1;
   const int H = L->H, I = L->I, E = L->E;
   if (L->fmt == MOE_FMT_NVFP4) {
     L->xb = H / 2; L->hb = I / 2; L->x_tiles_k = H / 64; L->h_tiles_k = I / 64;
@@ -376,9 +378,10 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   mark(3);
   const int64_t chunks = max_chunks(L, T);
   const int pair = L->pair_scale_copies && T <= kPairCopyMaxTokens;
-  if (e == cudaSuccess) e = run_gemm1(L, chunks, T, pair, s);
+  const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && T > kPairCopyMaxTokens);
+  if (e == cudaSuccess) e = run_gemm1(L, chunks, T, pair, wide, s);
   mark(4);
-  if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, L->y, 0, s);
+  if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, wide, L->y, 0, s);
   mark(5);
   if (e == cudaSuccess) e = launch_combine(L->y, L->inv, L->w, T, K, H, out, s);
   mark(6);
@@ -403,8 +406,9 @@ moe_status moe_forward_batched(moe_layer* L, const void* hidden, const int32_t* 
   cudaError_t e = launch_batched_quant(L->fmt, hidden, counts, M, L->E, L->H, L->counts,
                                        L->offsets, L->pad_off, L->chunk_off, L->xq, L->xsf,
                                        L->status, s);
-  if (e == cudaSuccess) e = run_gemm1(L, chunks, M, pair, s);
-  if (e == cudaSuccess) e = run_gemm2(L, chunks, M, pair, out, M, s);
+  const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && M >= 256);
+  if (e == cudaSuccess) e = run_gemm1(L, chunks, M, pair, wide, s);
+  if (e == cudaSuccess) e = run_gemm2(L, chunks, M, pair, wide, out, M, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   L->last_T = 0;
   L->last_launches = 3;

@@ -35,10 +35,23 @@ namespace moe {
 namespace {
 
 constexpr int kTileBytes = 128 * 128;  // 128 rows x 128 bytes of K
-constexpr int kAccCols = 128;          // TMEM columns per accumulator
 constexpr int kSfColBase = 256;        // TMEM columns for scale tiles
-constexpr int kSfColsPerStage = 32;
 constexpr int kTmemCols = 512;
+
+// NW = weight tiles (of 128 rows) per work item, i.e. the MMA's N / 128.
+// NW = 1: two 128-column accumulators (the epilogue of one item overlaps
+// the main loop of the next) and 32 scale columns per stage.  NW = 2 (wide
+// items, N = 256: half the shared-memory traffic per FLOP for the
+// activation operand): one 256-column accumulator and 64 scale columns per
+// stage (activation tile j at 16 j, weight tiles j at 16 j + 8 and
+// 16 j + 12 for NVFP4; MXFP8: weight tiles at 0 and 4, activation at 8).
+template <int NW>
+struct Wide {
+  static constexpr int kAccCols = 128 * NW;       // TMEM columns per accumulator
+  static constexpr int kBufs = NW == 1 ? 2 : 1;   // accumulators
+  static constexpr int kSfCols = 32 * NW;         // scale columns per stage
+  static constexpr int kMaxStages = (kTmemCols - kSfColBase) / kSfCols;
+};
 
 template <int FMT>
 struct Fmt;
@@ -55,33 +68,36 @@ struct Fmt<kFmtNVFP4> {
   static constexpr int kSfTiles = 4;  // 256 K elements = 16 x 16-blocks
 };
 
-// A stage holds the activation tile (MROWS rows x 128 bytes), the weight
-// tile (128 rows x 128 bytes) with its scale tiles right after it, and the
-// activation scale tiles.  MROWS is an upper bound on the real rows of any
-// chunk of the launch (rows per expert never exceed T), so decode launches
-// keep a short activation region and fit more stages.
-template <int FMT, int MROWS>
+// A stage holds the activation tile (MROWS rows x 128 bytes), the NW weight
+// tiles' codes (NW x 128 rows x 128 bytes, consecutive so they form one
+// 128*NW-row MMA operand), the weight tiles' scale tiles and the activation
+// scale tiles.  MROWS is an upper bound on the real rows of any chunk of
+// the launch (rows per expert never exceed T), so decode launches keep a
+// short activation region and fit more stages.
+template <int FMT, int MROWS, int NW>
 __host__ __device__ constexpr int stage_bytes() {
-  return MROWS * 128 + kTileBytes + 2 * Fmt<FMT>::kSfTiles * 512;
+  return MROWS * 128 + NW * kTileBytes + (NW + 1) * Fmt<FMT>::kSfTiles * 512;
 }
 
 // Per-expert item tables kept in shared memory: chunk_off[E+1],
 // pad_off[E], counts[E].
 constexpr int kTableInts = 3 * (kMaxExperts + 1);
 constexpr int kSmemLimit = 232448;  // opt-in maximum per block
-constexpr int kMaxStages = 8;       // TMEM holds 8 stages of scale columns
 
-template <int FMT, int MROWS>
+// Stages: as many as shared memory holds, at most as many as TMEM has scale
+// columns for.
+template <int FMT, int MROWS, int NW>
 __host__ __device__ constexpr int num_stages() {
-  return (kSmemLimit - 1024 - kTableInts * 4 - 256) / stage_bytes<FMT, MROWS>() > kMaxStages
-             ? kMaxStages
-             : (kSmemLimit - 1024 - kTableInts * 4 - 256) / stage_bytes<FMT, MROWS>();
+  return (kSmemLimit - 1024 - kTableInts * 4 - 256) / stage_bytes<FMT, MROWS, NW>() >
+                 Wide<NW>::kMaxStages
+             ? Wide<NW>::kMaxStages
+             : (kSmemLimit - 1024 - kTableInts * 4 - 256) / stage_bytes<FMT, MROWS, NW>();
 }
 
-template <int FMT, int MROWS>
+template <int FMT, int MROWS, int NW>
 __host__ __device__ constexpr int smem_bytes() {
-  return 1024 + num_stages<FMT, MROWS>() * stage_bytes<FMT, MROWS>() +
-         (2 * num_stages<FMT, MROWS>() + 5) * 8 + 16 + kTableInts * 4;
+  return 1024 + num_stages<FMT, MROWS, NW>() * stage_bytes<FMT, MROWS, NW>() +
+         (2 * num_stages<FMT, MROWS, NW>() + 5) * 8 + 16 + kTableInts * 4;
 }
 
 struct Item {
@@ -135,86 +151,79 @@ __device__ __forceinline__ float silu_mul(float g, float u, float L) {
 }
 
 // ---------------------------------------------------------------- epilogues
-// Thread = accumulator row (token row `prow`); columns 0..63 hold the gate
-// and 64..127 the up projection of intermediate features 64*n_tile + j.
+// Four 16-column TMEM loads (columns c0.., c1.., c2.., c3.. of this warp's
+// lanes) in flight together, then one wait: v[16 i + k] = column ci + k.
+__device__ __forceinline__ void tmem_ld_4x16(uint32_t base, int c0, int c1, int c2, int c3,
+                                             uint32_t (&v)[64]) {
+  auto part = [&](int i) -> uint32_t(&)[16] { return *reinterpret_cast<uint32_t(*)[16]>(&v[16 * i]); };
+  tmem_ld16(base + c0, part(0));
+  tmem_ld16(base + c1, part(1));
+  tmem_ld16(base + c2, part(2));
+  tmem_ld16(base + c3, part(3));
+  tmem_ld_wait();
+  reg_fence16(part(0));
+  reg_fence16(part(1));
+  reg_fence16(part(2));
+  reg_fence16(part(3));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 16 bf16 values (32 bytes) to dst.
+__device__ __forceinline__ void store_bf16x16(uint8_t* dst, const float* h) {
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(h[2 * i], h[2 * i + 1]);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// GEMM1: thread = accumulator row (token row `prow`); columns 0..63 hold the
+// gate and 64..127 the up projection of intermediate features 64*n_tile + j.
+// Each round loads the gate and up columns of 32 features (64 columns) with
+// one TMEM wait.
 template <int FMT>
 __device__ __forceinline__ void epilogue_gemm1(uint32_t taddr, bool store, int64_t prow,
                                                int n_tile, const GemmArgs& a) {
-  if constexpr (FMT == kFmtNVFP4) {
-    uint32_t packed[8];
-    uint32_t sf4 = 0;
 #pragma unroll
-    for (int jb = 0; jb < 4; ++jb) {
-      uint32_t g[16], u[16];
-      tmem_ld16(taddr + jb * 16, g);
-      tmem_ld16(taddr + 64 + jb * 16, u);
-      tmem_ld_wait();
-      reg_fence16(g);
-      reg_fence16(u);
-      float h[16];
+  for (int p = 0; p < 2; ++p) {
+    uint32_t v[64];  // gate 32p.. : v[0..31], up 32p.. : v[32..63]
+    tmem_ld_4x16(taddr, 32 * p, 32 * p + 16, 64 + 32 * p, 64 + 32 * p + 16, v);
+    float h[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) h[i] = silu_mul(lane_value(g[i], store), lane_value(u[i], store), a.clamp);
-      uint32_t c[2];
-      uint8_t sf;
-      quant_nvfp4_16(h, c, sf);
-      packed[2 * jb] = c[0];
-      packed[2 * jb + 1] = c[1];
-      sf4 |= static_cast<uint32_t>(sf) << (8 * jb);
-    }
-    if (store) {
-      uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 32);
-      dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-      *reinterpret_cast<uint32_t*>(a.out_sf + sf_tile_offset(prow, n_tile * 4, a.out_sf_tiles_k)) = sf4;
-    }
-  } else if constexpr (FMT == kFmtMXFP8) {
-#pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {
-      float h[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t g[16], u[16];
-        tmem_ld16(taddr + jb * 32 + half * 16, g);
-        tmem_ld16(taddr + 64 + jb * 32 + half * 16, u);
-        tmem_ld_wait();
-        reg_fence16(g);
-        reg_fence16(u);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          h[half * 16 + i] = silu_mul(lane_value(g[i], store), lane_value(u[i], store), a.clamp);
+    for (int i = 0; i < 32; ++i)
+      h[i] = silu_mul(lane_value(v[i], store), lane_value(v[32 + i], store), a.clamp);
+    if constexpr (FMT == kFmtNVFP4) {
+      uint32_t c[4];
+      uint8_t sf0, sf1;
+      quant_nvfp4_16(h, *reinterpret_cast<uint32_t(*)[2]>(&c[0]), sf0);
+      quant_nvfp4_16(h + 16, *reinterpret_cast<uint32_t(*)[2]>(&c[2]), sf1);
+      if (store) {
+        *reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 32 + p * 16) =
+            make_uint4(c[0], c[1], c[2], c[3]);
+        *reinterpret_cast<uint16_t*>(
+            a.out_sf + sf_tile_offset(prow, n_tile * 4 + 2 * p, a.out_sf_tiles_k)) =
+            static_cast<uint16_t>(sf0 | (sf1 << 8));
       }
+    } else if constexpr (FMT == kFmtMXFP8) {
       uint32_t c[8];
       uint8_t sf;
       quant_mxfp8_32(h, c, sf);
       if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + jb * 32);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + p * 32);
         dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
         dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-        a.out_sf[sf_tile_offset(prow, n_tile * 2 + jb, a.out_sf_tiles_k)] = sf;
+        a.out_sf[sf_tile_offset(prow, n_tile * 2 + p, a.out_sf_tiles_k)] = sf;
       }
-    }
-  } else {
-#pragma unroll
-    for (int jb = 0; jb < 4; ++jb) {
-      uint32_t g[16], u[16];
-      tmem_ld16(taddr + jb * 16, g);
-      tmem_ld16(taddr + 64 + jb * 16, u);
-      tmem_ld_wait();
-      reg_fence16(g);
-      reg_fence16(u);
-      uint32_t o[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float h0 = silu_mul(lane_value(g[2 * i], store), lane_value(u[2 * i], store), a.clamp);
-        const float h1 =
-            silu_mul(lane_value(g[2 * i + 1], store), lane_value(u[2 * i + 1], store), a.clamp);
-        const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
-        o[i] = *reinterpret_cast<const uint32_t*>(&b);
-      }
+    } else {
       if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + (n_tile * 64 + jb * 16) * 2);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        uint8_t* dst = a.out + prow * a.out_ld + (n_tile * 64 + p * 32) * 2;
+        store_bf16x16(dst, h);
+        store_bf16x16(dst + 32, h + 16);
       }
     }
   }
@@ -223,7 +232,7 @@ __device__ __forceinline__ void epilogue_gemm1(uint32_t taddr, bool store, int64
 // GEMM1 with the non-gated squared ReLU: thread = accumulator row; the 128
 // columns are intermediate features 128*n_tile + j, h = max(x, 0)^2 (one
 // correctly rounded fp32 product), then the same re-quantisation per 16-
-// (NVFP4) or 32- (MXFP8) block, or a bf16 round.
+// (NVFP4) or 32- (MXFP8) block, or a bf16 round.  64 columns per TMEM wait.
 __device__ __forceinline__ float relu_sq(float x) {
   x = fmaxf(x, 0.0f);
   return __fmul_rn(x, x);
@@ -232,112 +241,87 @@ __device__ __forceinline__ float relu_sq(float x) {
 template <int FMT>
 __device__ __forceinline__ void epilogue_relu2(uint32_t taddr, bool store, int64_t prow,
                                                int n_tile, const GemmArgs& a) {
-  if constexpr (FMT == kFmtNVFP4) {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t packed[8];
+  for (int half = 0; half < 2; ++half) {
+    uint32_t v[64];
+    tmem_ld_4x16(taddr, 64 * half, 64 * half + 16, 64 * half + 32, 64 * half + 48, v);
+    float h[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) h[i] = relu_sq(lane_value(v[i], store));
+    if constexpr (FMT == kFmtNVFP4) {
+      uint32_t c[8];
       uint32_t sf4 = 0;
 #pragma unroll
       for (int jb = 0; jb < 4; ++jb) {
-        uint32_t v[16];
-        tmem_ld16(taddr + half * 64 + jb * 16, v);
-        tmem_ld_wait();
-        reg_fence16(v);
-        float h[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) h[i] = relu_sq(lane_value(v[i], store));
-        uint32_t c[2];
         uint8_t sf;
-        quant_nvfp4_16(h, c, sf);
-        packed[2 * jb] = c[0];
-        packed[2 * jb + 1] = c[1];
+        quant_nvfp4_16(h + 16 * jb, *reinterpret_cast<uint32_t(*)[2]>(&c[2 * jb]), sf);
         sf4 |= static_cast<uint32_t>(sf) << (8 * jb);
       }
       if (store) {
         uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + half * 32);
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
         *reinterpret_cast<uint32_t*>(
             a.out_sf + sf_tile_offset(prow, n_tile * 8 + half * 4, a.out_sf_tiles_k)) = sf4;
       }
-    }
-  } else if constexpr (FMT == kFmtMXFP8) {
+    } else if constexpr (FMT == kFmtMXFP8) {
 #pragma unroll
-    for (int jb = 0; jb < 4; ++jb) {
-      float h[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[16];
-        tmem_ld16(taddr + jb * 32 + half * 16, v);
-        tmem_ld_wait();
-        reg_fence16(v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) h[half * 16 + i] = relu_sq(lane_value(v[i], store));
+      for (int jb = 0; jb < 2; ++jb) {
+        uint32_t c[8];
+        uint8_t sf;
+        quant_mxfp8_32(h + 32 * jb, c, sf);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 128 +
+                                                half * 64 + jb * 32);
+          dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+          dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+          a.out_sf[sf_tile_offset(prow, n_tile * 4 + half * 2 + jb, a.out_sf_tiles_k)] = sf;
+        }
       }
-      uint32_t c[8];
-      uint8_t sf;
-      quant_mxfp8_32(h, c, sf);
+    } else {
       if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 128 + jb * 32);
-        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-        a.out_sf[sf_tile_offset(prow, n_tile * 4 + jb, a.out_sf_tiles_k)] = sf;
-      }
-    }
-  } else {
+        uint8_t* dst = a.out + prow * a.out_ld + (n_tile * 128 + half * 64) * 2;
 #pragma unroll
-    for (int jb = 0; jb < 8; ++jb) {
-      uint32_t v[16];
-      tmem_ld16(taddr + jb * 16, v);
-      tmem_ld_wait();
-      reg_fence16(v);
-      uint32_t o[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(relu_sq(lane_value(v[2 * i], store)),
-                                                       relu_sq(lane_value(v[2 * i + 1], store)));
-        o[i] = *reinterpret_cast<const uint32_t*>(&b);
-      }
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + (n_tile * 128 + jb * 16) * 2);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        for (int q = 0; q < 4; ++q) store_bf16x16(dst + 32 * q, h + 16 * q);
       }
     }
   }
 }
 
-// GEMM2: 128 output features per row, stored as bf16.
+// GEMM2: 128 output features per row, stored as bf16; 64 columns per TMEM
+// wait.
 __device__ __forceinline__ void epilogue_gemm2(uint32_t taddr, bool store, int64_t prow,
                                                int n_tile, const GemmArgs& a) {
 #pragma unroll
-  for (int jb = 0; jb < 8; ++jb) {
-    uint32_t v[16];
-    tmem_ld16(taddr + jb * 16, v);
-    tmem_ld_wait();
-    reg_fence16(v);
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-      o[i] = *reinterpret_cast<const uint32_t*>(&b);
-    }
+  for (int half = 0; half < 2; ++half) {
+    uint32_t v[64];
+    tmem_ld_4x16(taddr, 64 * half, 64 * half + 16, 64 * half + 32, 64 * half + 48, v);
     if (store) {
-      uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + (n_tile * 128 + jb * 16) * 2);
-      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + (n_tile * 128 + half * 64) * 2);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
     }
   }
 }
 
 // ---------------------------------------------------------------- kernel
-template <int FMT, int EPI, int MROWS>
+template <int FMT, int EPI, int MROWS, int NW>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   constexpr int SFT = Fmt<FMT>::kSfTiles;
-  constexpr int SB = stage_bytes<FMT, MROWS>();
-  constexpr int kStages = num_stages<FMT, MROWS>();
+  constexpr int SB = stage_bytes<FMT, MROWS, NW>();
+  constexpr int kStages = num_stages<FMT, MROWS, NW>();
   constexpr int A_BYTES = MROWS * 128;
+  constexpr int kAccCols = Wide<NW>::kAccCols;
+  constexpr int kBufs = Wide<NW>::kBufs;
+  constexpr int kSfColsPerStage = Wide<NW>::kSfCols;
+  // shared-memory offsets inside a stage
+  constexpr int kOffBsf = A_BYTES + NW * kTileBytes;        // weight scale tiles
+  constexpr int kOffAsf = kOffBsf + NW * SFT * 512;          // activation scale tiles
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * SB);
@@ -387,10 +371,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      // A weight tile read by one chunk only (decode) is dead after this
-      // read; one read by several chunks of its expert stays in L2 for them.
-      const uint64_t pol_once = l2_policy_evict_first(), pol_shared = l2_policy_evict_normal();
-      const int pf = args.l2_prefetch;
+      const uint64_t policy = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -402,26 +383,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t bytes = (16u << amap) * 128u + args.b_tile_bytes + SFT * 512u;
+        const uint32_t bytes = (16u << amap) * 128u + NW * args.b_tile_bytes + SFT * 512u;
         const uint8_t* sfa = args.sfa + static_cast<int64_t>(it.prow0 >> 7) * args.sfa_tiles_k * 512;
+        // the item's first 128-row weight tile; the next one (NW = 2)
+        // follows num_kb tiles later
         const uint8_t* btile =
-            args.b_tiles + (static_cast<int64_t>(it.e) * args.n_tiles + it.n_tile) * args.num_kb *
-                               args.b_tile_bytes;
-        const uint64_t policy =
-            tab.chunk_off[it.e + 1] - tab.chunk_off[it.e] > 1 ? pol_shared : pol_once;
-        // Warm L2 with the operands of the stages `pf` ahead of the ring:
-        // the copies then find them in L2 instead of waiting on HBM (many
-        // CTAs read the same weight tile at about the same time).
-        for (int kb = 0; kb < pf && kb < args.num_kb; ++kb) {
-          prefetch_l2(btile + static_cast<int64_t>(kb) * args.b_tile_bytes, args.b_tile_bytes);
-          prefetch_l2_tile(&maps.a[amap], kb * 128, it.prow0);
-        }
+            args.b_tiles + (static_cast<int64_t>(it.e) * args.n_tiles + it.n_tile) * NW *
+                               args.num_kb * args.b_tile_bytes;
         for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (pf && kb + pf < args.num_kb) {
-            prefetch_l2(btile + static_cast<int64_t>(kb + pf) * args.b_tile_bytes,
-                        args.b_tile_bytes);
-            prefetch_l2_tile(&maps.a[amap], (kb + pf) * 128, it.prow0);
-          }
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -429,12 +398,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sp = smem + stage * SB;
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sp, &maps.a[amap], &full[stage], kb * 128, it.prow0);
-          // weight tile codes + its scale tiles: one contiguous block
-          bulk_load_hint(sp + A_BYTES, btile + static_cast<int64_t>(kb) * args.b_tile_bytes,
-                         args.b_tile_bytes, &full[stage], policy);
+          if constexpr (NW == 1) {
+            // weight tile codes + its scale tiles: one contiguous block
+            bulk_load_hint(sp + A_BYTES, btile + static_cast<int64_t>(kb) * args.b_tile_bytes,
+                           args.b_tile_bytes, &full[stage], policy);
+          } else {
+            // codes of both tiles back to back (one 256-row operand), then
+            // their scale tiles
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+              const uint8_t* src =
+                  btile + (static_cast<int64_t>(w) * args.num_kb + kb) * args.b_tile_bytes;
+              bulk_load_hint(sp + A_BYTES + w * kTileBytes, src, kTileBytes, &full[stage], policy);
+              if constexpr (SFT > 0)
+                bulk_load_hint(sp + kOffBsf + w * SFT * 512, src + kTileBytes, SFT * 512,
+                               &full[stage], policy);
+            }
+          }
           if constexpr (SFT > 0)
-            bulk_load(sp + A_BYTES + kTileBytes + SFT * 512, sfa + kb * SFT * 512, SFT * 512,
-                      &full[stage]);
+            bulk_load(sp + kOffAsf, sfa + kb * SFT * 512, SFT * 512, &full[stage]);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -454,16 +436,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t idesc;
-      if constexpr (FMT == kFmtBF16) idesc = idesc_bf16(128, 128);
-      else if constexpr (FMT == kFmtNVFP4) idesc = idesc_nvf4(128, 128);
+      if constexpr (FMT == kFmtBF16) idesc = idesc_bf16(128, 128 * NW);
+      else if constexpr (FMT == kFmtNVFP4) idesc = idesc_nvf4(128, 128 * NW);
       else idesc = 0;
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++local) {
-        const int buf = local & 1;
-        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        const int buf = local % kBufs;
+        const uint32_t use = static_cast<uint32_t>(local / kBufs);
         // A chunk of at most 32 rows keeps all its real accumulator rows in
         // TMEM lane quarter 0.  The MMA of each lane quarter reads both
         // operands' scales from that quarter's own lanes, so then only lanes
@@ -471,8 +453,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // non-broadcast 128x256b copy (the other lanes receive neighbouring
         // shared memory and only feed accumulator rows that are not stored).
         // Larger chunks broadcast every tile to all four quarters.
-        const bool q0_only =
-            args.pair_scale_copies && map_item(tab, args.E, args.n_tiles, item).rows <= 32;
+        const bool q0_only = NW == 1 && args.pair_scale_copies &&
+                             map_item(tab, args.E, args.n_tiles, item).rows <= 32;
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -487,9 +469,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           uint8_t* sp = smem + stage * SB;
           const uint32_t a_addr = smem_u32(sp), b_addr = smem_u32(sp + A_BYTES);
-          uint8_t* sf = sp + A_BYTES + kTileBytes;  // weight scales, then activation scales
+          uint8_t* sf = sp + kOffBsf;  // weight scales, then activation scales
           const uint32_t sf_col = tmem + kSfColBase + stage * kSfColsPerStage;
-          if constexpr (FMT == kFmtNVFP4) {
+          if constexpr (FMT == kFmtNVFP4 && NW == 2) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tc_copy_sf(sf_col + j * 16, desc_sf(smem_u32(sp + kOffAsf + j * 512)));
+              tc_copy_sf(sf_col + j * 16 + 8, desc_sf(smem_u32(sf + j * 512)));
+              tc_copy_sf(sf_col + j * 16 + 12, desc_sf(smem_u32(sf + (SFT + j) * 512)));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                       sf_col + j * 16, sf_col + j * 16 + 8, (kb | j) != 0);
+          } else if constexpr (FMT == kFmtMXFP8 && NW == 2) {
+            tc_copy_sf(sf_col, desc_sf(smem_u32(sf)));
+            tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf + 512)));
+            tc_copy_sf(sf_col + 8, desc_sf(smem_u32(sp + kOffAsf)));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
+                       idesc_mxf8(128, 256, j), sf_col + 8, sf_col, (kb | j) != 0);
+          } else if constexpr (FMT == kFmtNVFP4) {
             if (q0_only) {
               // columns: A scales of substeps 0-1 | 2-3, B scales 0-1 | 2-3
               const uint32_t sfa = smem_u32(sf + 4 * 512), sfb = smem_u32(sf);
@@ -551,8 +552,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int local = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++local) {
       const Item it = map_item(tab, args.E, args.n_tiles, item);
-      const int buf = local & 1;
-      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      const int buf = local % kBufs;
+      const uint32_t use = static_cast<uint32_t>(local / kBufs);
       if (!mbar_wait(&tfull[buf], use & 1u, abort_flag)) {
         if (lane == 0) report_status(args.status, kStatusTimeout);
         break;
@@ -560,18 +561,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int r = q * 32 + lane;
       if (q * 32 < it.rows) {
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols;
+        const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols;
         const int64_t prow = it.prow0 + r;
-        if constexpr (EPI == 1) epilogue_gemm1<FMT>(taddr, r < it.rows, prow, it.n_tile, args);
-        else if constexpr (EPI == 3) epilogue_relu2<FMT>(taddr, r < it.rows, prow, it.n_tile, args);
-        else {
-          // batched format: expert e's rows go to rows e*M.. of the output
-          const int64_t orow =
-              args.out_rows_per_expert
-                  ? static_cast<int64_t>(it.e) * args.out_rows_per_expert +
-                        (it.prow0 - tab.pad_off[it.e]) + r
-                  : prow;
-          epilogue_gemm2(taddr, r < it.rows, orow, it.n_tile, args);
+        // batched format: expert e's rows go to rows e*M.. of the output
+        const int64_t orow = args.out_rows_per_expert
+                                 ? static_cast<int64_t>(it.e) * args.out_rows_per_expert +
+                                       (it.prow0 - tab.pad_off[it.e]) + r
+                                 : prow;
+#pragma unroll
+        for (int g = 0; g < NW; ++g) {  // one 128-column group per weight tile
+          const uint32_t taddr = tbase + g * 128;
+          const int n128 = it.n_tile * NW + g;
+          if constexpr (EPI == 1) epilogue_gemm1<FMT>(taddr, r < it.rows, prow, n128, args);
+          else if constexpr (EPI == 3) epilogue_relu2<FMT>(taddr, r < it.rows, prow, n128, args);
+          else epilogue_gemm2(taddr, r < it.rows, orow, n128, args);
         }
       }
       tc_fence_before();
@@ -586,39 +589,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int FMT, int EPI, int MROWS>
+template <int FMT, int EPI, int MROWS, int NW>
 cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t s) {
-  return launch_pdl(g_pdl_gemm, moe_gemm_kernel<FMT, EPI, MROWS>, dim3(grid),
-                    dim3(kGemmThreads), smem_bytes<FMT, MROWS>(), s, maps, args);
+  return launch_pdl(g_pdl_gemm, moe_gemm_kernel<FMT, EPI, MROWS, NW>, dim3(grid),
+                    dim3(kGemmThreads), smem_bytes<FMT, MROWS, NW>(), s, maps, args);
 }
 
-template <int FMT, int MROWS>
+template <int FMT, int EPI, int MROWS, int NW>
+cudaError_t set_smem() {
+  return cudaFuncSetAttribute(moe_gemm_kernel<FMT, EPI, MROWS, NW>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes<FMT, MROWS, NW>());
+}
+
+template <int FMT, int MROWS, int NW>
 cudaError_t prepare_m() {
-  cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<FMT, 1, MROWS>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes<FMT, MROWS>());
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(moe_gemm_kernel<FMT, 3, MROWS>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<FMT, MROWS>());
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(moe_gemm_kernel<FMT, 2, MROWS>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<FMT, MROWS>());
+  cudaError_t e = set_smem<FMT, 1, MROWS, NW>();
+  if (e == cudaSuccess) e = set_smem<FMT, 2, MROWS, NW>();
+  if (e == cudaSuccess) e = set_smem<FMT, 3, MROWS, NW>();
+  return e;
 }
 
 template <int FMT>
 cudaError_t prepare_one() {
-  cudaError_t e = prepare_m<FMT, 32>();
-  if (e == cudaSuccess) e = prepare_m<FMT, 64>();
-  if (e == cudaSuccess) e = prepare_m<FMT, 128>();
+  cudaError_t e = prepare_m<FMT, 32, 1>();
+  if (e == cudaSuccess) e = prepare_m<FMT, 64, 1>();
+  if (e == cudaSuccess) e = prepare_m<FMT, 128, 1>();
+  if (e == cudaSuccess) e = prepare_m<FMT, 128, 2>();
   return e;
 }
 
 template <int FMT, int EPI>
-cudaError_t launch_fmt(const GemmMaps& maps, const GemmArgs& args, int grid, int mrows,
+cudaError_t launch_fmt(const GemmMaps& maps, const GemmArgs& args, int grid, int mrows, bool wide,
                        cudaStream_t s) {
-  if (mrows <= 32) return launch_one<FMT, EPI, 32>(maps, args, grid, s);
-  if (mrows <= 64) return launch_one<FMT, EPI, 64>(maps, args, grid, s);
-  return launch_one<FMT, EPI, 128>(maps, args, grid, s);
+  if (wide) return launch_one<FMT, EPI, 128, 2>(maps, args, grid, s);
+  if (mrows <= 32) return launch_one<FMT, EPI, 32, 1>(maps, args, grid, s);
+  if (mrows <= 64) return launch_one<FMT, EPI, 64, 1>(maps, args, grid, s);
+  return launch_one<FMT, EPI, 128, 1>(maps, args, grid, s);
+}
+
+template <int FMT>
+cudaError_t launch_epi(int epi, const GemmMaps& maps, const GemmArgs& args, int grid, int mrows,
+                       bool wide, cudaStream_t s) {
+  return epi == 1   ? launch_fmt<FMT, 1>(maps, args, grid, mrows, wide, s)
+         : epi == 3 ? launch_fmt<FMT, 3>(maps, args, grid, mrows, wide, s)
+                    : launch_fmt<FMT, 2>(maps, args, grid, mrows, wide, s);
 }
 
 }  // namespace
@@ -630,18 +645,10 @@ cudaError_t gemm_prepare(int fmt) {
 }
 
 cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& args, int grid,
-                        int max_rows, cudaStream_t s) {
-  if (fmt == kFmtBF16)
-    return epi == 1   ? launch_fmt<kFmtBF16, 1>(maps, args, grid, max_rows, s)
-           : epi == 3 ? launch_fmt<kFmtBF16, 3>(maps, args, grid, max_rows, s)
-                      : launch_fmt<kFmtBF16, 2>(maps, args, grid, max_rows, s);
-  if (fmt == kFmtMXFP8)
-    return epi == 1   ? launch_fmt<kFmtMXFP8, 1>(maps, args, grid, max_rows, s)
-           : epi == 3 ? launch_fmt<kFmtMXFP8, 3>(maps, args, grid, max_rows, s)
-                      : launch_fmt<kFmtMXFP8, 2>(maps, args, grid, max_rows, s);
-  return epi == 1   ? launch_fmt<kFmtNVFP4, 1>(maps, args, grid, max_rows, s)
-         : epi == 3 ? launch_fmt<kFmtNVFP4, 3>(maps, args, grid, max_rows, s)
-                    : launch_fmt<kFmtNVFP4, 2>(maps, args, grid, max_rows, s);
+                        int max_rows, bool wide, cudaStream_t s) {
+  if (fmt == kFmtBF16) return launch_epi<kFmtBF16>(epi, maps, args, grid, max_rows, wide, s);
+  if (fmt == kFmtMXFP8) return launch_epi<kFmtMXFP8>(epi, maps, args, grid, max_rows, wide, s);
+  return launch_epi<kFmtNVFP4>(epi, maps, args, grid, max_rows, wide, s);
 }
 
 }  // namespace moe

@@ -47,7 +47,6 @@ struct GemmArgs {
   int out_sf_tiles_k;
   float clamp;               // +inf: no clamp
   int pair_scale_copies;     // 1: chunks of <= 32 rows copy scales to lanes 0-31 only
-  int l2_prefetch;           // stages ahead whose operands are prefetched into L2 (0: off)
   int out_rows_per_expert;   // 0: output row = padded row; M > 0 (batched format):
                              // output row = e * M + row within the expert
   int* status;
@@ -103,9 +102,11 @@ cudaError_t gemm_prepare(int fmt);  // raise the dynamic shared-memory limit
 // max_rows: upper bound on the rows of any expert in this launch (<= T);
 // selects the activation-tile height of the shared-memory stages.
 // epi: 1 = GEMM1 + SwiGLU, 3 = GEMM1 + ReLU^2 (both re-quantise into the
-// GEMM2 input format), 2 = GEMM2 (bf16 out).
+// GEMM2 input format), 2 = GEMM2 (bf16 out).  wide: items of two 128-row
+// weight tiles (MMA N = 256; args.n_tiles counts those pairs), for launches
+// whose chunks are mostly full 128-row blocks.
 cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& args, int grid,
-                        int max_rows, cudaStream_t s);
+                        int max_rows, bool wide, cudaStream_t s);
 
 // Routing, permutation + activation quantisation, combine.
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* w,

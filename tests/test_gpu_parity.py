@@ -323,3 +323,53 @@ def test_batched_capacity_and_arguments():
         moe_forward_batched(layer.handle, hid, cnt, -1, hid)
     assert e.value.code == 1
     layer.close()
+
+
+# ---- GEMM items of two weight tiles (N = 256), used for prefill-sized T -------
+@pytest.mark.parametrize("name,over,force", [
+    ("bf16_small", dict(), True),
+    ("mxfp8_small", dict(), True),
+    ("nvfp4_small", dict(), True),
+    ("nvfp4_small", dict(T=200, E=3, K=2), True),
+    ("nvfp4_small", dict(act="relu2"), True),
+    ("mxfp8_small", dict(act="relu2", T=150, E=4, K=2), True),
+    ("nvfp4_zipf_small", dict(T=1100, E=24, K=4), False),   # T > 1024 selects them itself
+], ids=["bf16", "mxfp8", "nvfp4", "nvfp4-chunks", "nvfp4-relu2", "mxfp8-relu2", "nvfp4-T1100"])
+def test_wide_items_match_oracle(name, over, force, monkeypatch):
+    if force:
+        monkeypatch.setenv("MOE_WIDE_TILES", "1")
+    s = workloads.spec(name, **over)
+    case = workloads.make_case(s, seed=12)
+    ref = run_oracle(s, case, intermediates=True)
+    layer = make_layer(s, weights=case["weights"])
+    out = run_gpu(layer, case["hidden"], case["logits"])
+    assert layer.status() == 0
+    h, y = (t.cpu().numpy() for t in layer.intermediates())
+    assert rel_l2(h, ref["h"]) <= TOL[s["fmt"]], "GEMM2 input"
+    assert rel_l2(y, ref["y"]) <= TOL[s["fmt"]], "GEMM2 output"
+    assert rel_l2(out.float().cpu().numpy(), bf16_bits_to_f64(ref["out"])) <= TOL[s["fmt"]]
+    layer.close()
+
+
+def test_wide_items_batched_format(monkeypatch):
+    import oracle
+    from tests.gpu_helpers import cfg_of
+    monkeypatch.setenv("MOE_WIDE_TILES", "1")
+    s = workloads.spec("nvfp4_small", E=5)
+    M = 260
+    case = workloads.make_case(s, T=1, seed=13)
+    hid, counts = workloads.draw_batched(s, M, seed=13)
+    hb = hid.view(torch.int16).numpy().view("uint16")
+    ref = oracle.forward_batched(cfg_of(s), workloads.to_numpy_case(case)["weights"], hb,
+                                 counts.numpy(), want_y=True)
+    layer = make_layer(s, max_tokens=s["E"] * 384 // s["K"], weights=case["weights"])
+    out = layer.forward_batched(hid.cuda(), counts.cuda())
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    cn = counts.numpy()
+    got = out.float().cpu().numpy()
+    mask = np.zeros(got.shape[:2], bool)
+    for e in range(s["E"]):
+        mask[e, :cn[e]] = True
+    assert rel_l2(got[mask], ref["y"][mask]) <= TOL["nvfp4"]
+    layer.close()

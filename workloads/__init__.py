@@ -21,7 +21,8 @@ and a tie-to-even threshold table for e2m1.
 Workloads (sizes, distributions) follow the five layer configurations of this
 project: a tiny BF16 layer, a BF16 layer with clamp, an MXFP8 decode layer,
 an NVFP4 decode sweep and an NVFP4 prefill layer with Zipf(1.1) expert
-popularity.  Nothing here reads a dataset; every tensor is synthetic.
+popularity; plus a 32K-token NVFP4 prefill with uniform routing, where the
+tensor pipe rather than the weight bytes sets the pace.  Nothing here reads a dataset; every tensor is synthetic.
 """
 import math
 
@@ -40,6 +41,10 @@ CONFIGS = {
                          sweep=(1, 8, 32, 128)),
     "nvfp4_prefill": dict(T=8192, H=7168, I=2048, E=384, K=8, fmt="nvfp4",
                           clamp=0.0, wdist=0.02, logits="zipf1.1"),
+    # a prefill large enough that the FP4 tensor pipe, not the weight bytes,
+    # sets the pace: 262,144 routed rows over all 384 experts (~680 each)
+    "nvfp4_prefill_32k": dict(T=32768, H=7168, I=2048, E=384, K=8, fmt="nvfp4",
+                              clamp=0.0, wdist=0.02, logits="normal"),
 }
 
 # Reduced shapes of the same recipes for parity tests the oracle finishes in
