@@ -49,6 +49,7 @@ struct moe_layer {
   GemmMaps maps1{}, maps2{};
   int pair_scale_copies = 1;
   int wide_tiles = -1;               // 0 off, 1 always, -1 for prefill-sized launches
+  int stage_scales = 1;              // decode scales written by a warp, not copied
   bool weights_ready = false;
   int last_T = 0, last_launches = 0;
   std::vector<cudaEvent_t> tev;  // per-kernel timing events, 7 per forward
@@ -117,9 +118,7 @@ void free_all(moe_layer* L) {
 
 // Launches of more than kPairCopyMaxTokens tokens (mostly full 128-row
 // chunks) use GEMM items of two weight tiles (N = 256), which halves the
-// shared-memory traffic of the activation operand per FLOP.  BF16 and NVFP4
-// only: with the MXFP8 kind at N = 256 the second weight tile's scales are
-// not where the MMA reads them (results wrong), so MXFP8 keeps N = 128.
+// shared-memory traffic of the activation operand per FLOP.
 //
 // Chunks of at most 32 rows can take their block scales in with half as
 // many TMEM copies (lanes 0-31 only).  Measured on GB300 this speeds up
@@ -138,7 +137,7 @@ int64_t max_chunks(const moe_layer* L, int T) {
 // expert (selects the activation tile height).
 cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide,
                       cudaStream_t s) {
-  wide = wide && L->w13_rows % 256 == 0 && L->fmt != MOE_FMT_MXFP8;
+  wide = wide && L->w13_rows % 256 == 0;
   GemmArgs a{};
   a.chunk_off = L->chunk_off;
   a.pad_off = L->pad_off;
@@ -156,6 +155,7 @@ cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
   a.out_sf_tiles_k = L->h_tiles_k;
   a.clamp = L->clamp;
   a.pair_scale_copies = pair;
+  a.stage_scales = L->stage_scales;
   a.out_rows_per_expert = 0;
   a.status = L->status;
   const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
@@ -167,7 +167,7 @@ cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
 // rows e*rows_per_expert + i (batched format).
 cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide, void* out,
                       int rows_per_expert, cudaStream_t s) {
-  wide = wide && L->H % 256 == 0 && L->fmt != MOE_FMT_MXFP8;
+  wide = wide && L->H % 256 == 0;
   GemmArgs a{};
   a.chunk_off = L->chunk_off;
   a.pad_off = L->pad_off;
@@ -185,6 +185,7 @@ cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
   a.out_sf_tiles_k = 0;
   a.clamp = INFINITY;
   a.pair_scale_copies = pair;
+  a.stage_scales = L->stage_scales;
   a.out_rows_per_expert = rows_per_expert;
   a.status = L->status;
   const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
@@ -274,6 +275,9 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   // MOE_WIDE_TILES=0|1: never / always use the N = 256 GEMM items (default:
   // for launches of more than kPairCopyMaxTokens tokens).
   if (const char* wv = std::getenv("MOE_WIDE_TILES")) L->wide_tiles = wv[0] == '0' ? 0 : 1;
+  // MOE_SCALE_STAGER=0: decode chunks copy their scales with tcgen05.cp
+  // (lanes 0-31 through 128x256b copies) instead of a staging warp.
+  if (const char* sv = std::getenv("MOE_SCALE_STAGER")) L->stage_scales = sv[0] != '0';
   const int H = L->H, I = L->I, E = L->E;
   if (L->fmt == MOE_FMT_NVFP4) {
     L->xb = H / 2; L->hb = I / 2; L->x_tiles_k = H / 64; L->h_tiles_k = I / 64;

@@ -74,9 +74,12 @@ struct Fmt<kFmtNVFP4> {
 // scale tiles.  MROWS is an upper bound on the real rows of any chunk of
 // the launch (rows per expert never exceed T), so decode launches keep a
 // short activation region and fit more stages.
+// Rounded up to 1 KiB: the operand tiles at the start of every stage must
+// sit on 128-byte-swizzle atom boundaries.
 template <int FMT, int MROWS, int NW>
 __host__ __device__ constexpr int stage_bytes() {
-  return MROWS * 128 + NW * kTileBytes + (NW + 1) * Fmt<FMT>::kSfTiles * 512;
+  return (MROWS * 128 + NW * kTileBytes + (NW + 1) * Fmt<FMT>::kSfTiles * 512 + 1023) / 1024 *
+         1024;
 }
 
 // Per-expert item tables kept in shared memory: chunk_off[E+1],
@@ -97,8 +100,12 @@ __host__ __device__ constexpr int num_stages() {
 template <int FMT, int MROWS, int NW>
 __host__ __device__ constexpr int smem_bytes() {
   return 1024 + num_stages<FMT, MROWS, NW>() * stage_bytes<FMT, MROWS, NW>() +
-         (2 * num_stages<FMT, MROWS, NW>() + 5) * 8 + 16 + kTableInts * 4;
+         (3 * num_stages<FMT, MROWS, NW>() + 5) * 8 + 16 + kTableInts * 4;
 }
+
+// Warp 0 stages decode scales into TMEM lane quarter 0, warp 1 issues the
+// MMAs, warp 2 the copies, then four epilogue warps per 128-column group.
+__host__ __device__ constexpr int gemm_threads(int nw) { return 96 + 128 * nw; }
 
 struct Item {
   int e, n_tile, prow0, rows;
@@ -151,20 +158,26 @@ __device__ __forceinline__ float silu_mul(float g, float u, float L) {
 }
 
 // ---------------------------------------------------------------- epilogues
-// Four 16-column TMEM loads (columns c0.., c1.., c2.., c3.. of this warp's
-// lanes) in flight together, then one wait: v[16 i + k] = column ci + k.
-__device__ __forceinline__ void tmem_ld_4x16(uint32_t base, int c0, int c1, int c2, int c3,
-                                             uint32_t (&v)[64]) {
-  auto part = [&](int i) -> uint32_t(&)[16] { return *reinterpret_cast<uint32_t(*)[16]>(&v[16 * i]); };
-  tmem_ld16(base + c0, part(0));
-  tmem_ld16(base + c1, part(1));
-  tmem_ld16(base + c2, part(2));
-  tmem_ld16(base + c3, part(3));
-  tmem_ld_wait();
-  reg_fence16(part(0));
-  reg_fence16(part(1));
-  reg_fence16(part(2));
-  reg_fence16(part(3));
+// An epilogue covers one 128-column accumulator group in two rounds of 64
+// columns.  Narrow items (two accumulators) load each round just before
+// computing it; wide items load both rounds first and release their single
+// accumulator before computing, so the next item's MMAs can start.
+//
+// Columns of round p: GEMM1 + SwiGLU reads gate and up of 32 features
+// (gate 32p.., up 64+32p..); the other epilogues read columns 64p.. .
+template <int EPI>
+__device__ __forceinline__ void epilogue_load(uint32_t taddr, int p, uint32_t* v) {
+  const int c0 = EPI == 1 ? 32 * p : 64 * p;
+  const int c2 = EPI == 1 ? 64 + 32 * p : 64 * p + 32;
+  tmem_ld16(taddr + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+  tmem_ld16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+  tmem_ld16(taddr + c2, *reinterpret_cast<uint32_t(*)[16]>(v + 32));
+  tmem_ld16(taddr + c2 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 48));
+}
+
+__device__ __forceinline__ void epilogue_fence(uint32_t* v) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * i));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -182,135 +195,124 @@ __device__ __forceinline__ void store_bf16x16(uint8_t* dst, const float* h) {
   d[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// GEMM1: thread = accumulator row (token row `prow`); columns 0..63 hold the
-// gate and 64..127 the up projection of intermediate features 64*n_tile + j.
-// Each round loads the gate and up columns of 32 features (64 columns) with
-// one TMEM wait.
+// GEMM1 + SwiGLU, round p: thread = accumulator row (token row `prow`);
+// v[0..31] gate and v[32..63] up of intermediate features 64*n_tile + 32p + j.
 template <int FMT>
-__device__ __forceinline__ void epilogue_gemm1(uint32_t taddr, bool store, int64_t prow,
+__device__ __forceinline__ void epilogue_gemm1(const uint32_t* v, int p, bool store, int64_t prow,
                                                int n_tile, const GemmArgs& a) {
+  float h[32];
 #pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    uint32_t v[64];  // gate 32p.. : v[0..31], up 32p.. : v[32..63]
-    tmem_ld_4x16(taddr, 32 * p, 32 * p + 16, 64 + 32 * p, 64 + 32 * p + 16, v);
-    float h[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      h[i] = silu_mul(lane_value(v[i], store), lane_value(v[32 + i], store), a.clamp);
-    if constexpr (FMT == kFmtNVFP4) {
-      uint32_t c[4];
-      uint8_t sf0, sf1;
-      quant_nvfp4_16(h, *reinterpret_cast<uint32_t(*)[2]>(&c[0]), sf0);
-      quant_nvfp4_16(h + 16, *reinterpret_cast<uint32_t(*)[2]>(&c[2]), sf1);
-      if (store) {
-        *reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 32 + p * 16) =
-            make_uint4(c[0], c[1], c[2], c[3]);
-        *reinterpret_cast<uint16_t*>(
-            a.out_sf + sf_tile_offset(prow, n_tile * 4 + 2 * p, a.out_sf_tiles_k)) =
-            static_cast<uint16_t>(sf0 | (sf1 << 8));
-      }
-    } else if constexpr (FMT == kFmtMXFP8) {
-      uint32_t c[8];
-      uint8_t sf;
-      quant_mxfp8_32(h, c, sf);
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + p * 32);
-        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-        a.out_sf[sf_tile_offset(prow, n_tile * 2 + p, a.out_sf_tiles_k)] = sf;
-      }
-    } else {
-      if (store) {
-        uint8_t* dst = a.out + prow * a.out_ld + (n_tile * 64 + p * 32) * 2;
-        store_bf16x16(dst, h);
-        store_bf16x16(dst + 32, h + 16);
-      }
+  for (int i = 0; i < 32; ++i)
+    h[i] = silu_mul(lane_value(v[i], store), lane_value(v[32 + i], store), a.clamp);
+  if constexpr (FMT == kFmtNVFP4) {
+    uint32_t c[4];
+    uint8_t sf0, sf1;
+    quant_nvfp4_16(h, *reinterpret_cast<uint32_t(*)[2]>(&c[0]), sf0);
+    quant_nvfp4_16(h + 16, *reinterpret_cast<uint32_t(*)[2]>(&c[2]), sf1);
+    if (store) {
+      *reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 32 + p * 16) =
+          make_uint4(c[0], c[1], c[2], c[3]);
+      *reinterpret_cast<uint16_t*>(
+          a.out_sf + sf_tile_offset(prow, n_tile * 4 + 2 * p, a.out_sf_tiles_k)) =
+          static_cast<uint16_t>(sf0 | (sf1 << 8));
+    }
+  } else if constexpr (FMT == kFmtMXFP8) {
+    uint32_t c[8];
+    uint8_t sf;
+    quant_mxfp8_32(h, c, sf);
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + p * 32);
+      dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+      dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+      a.out_sf[sf_tile_offset(prow, n_tile * 2 + p, a.out_sf_tiles_k)] = sf;
+    }
+  } else {
+    if (store) {
+      uint8_t* dst = a.out + prow * a.out_ld + (n_tile * 64 + p * 32) * 2;
+      store_bf16x16(dst, h);
+      store_bf16x16(dst + 32, h + 16);
     }
   }
 }
 
-// GEMM1 with the non-gated squared ReLU: thread = accumulator row; the 128
-// columns are intermediate features 128*n_tile + j, h = max(x, 0)^2 (one
-// correctly rounded fp32 product), then the same re-quantisation per 16-
-// (NVFP4) or 32- (MXFP8) block, or a bf16 round.  64 columns per TMEM wait.
+// GEMM1 with the non-gated squared ReLU, round p: v holds intermediate
+// features 128*n_tile + 64p + j; h = max(x, 0)^2 (one correctly rounded fp32
+// product), then the same re-quantisation per 16- (NVFP4) or 32- (MXFP8)
+// block, or a bf16 round.
 __device__ __forceinline__ float relu_sq(float x) {
   x = fmaxf(x, 0.0f);
   return __fmul_rn(x, x);
 }
 
 template <int FMT>
-__device__ __forceinline__ void epilogue_relu2(uint32_t taddr, bool store, int64_t prow,
+__device__ __forceinline__ void epilogue_relu2(const uint32_t* v, int p, bool store, int64_t prow,
                                                int n_tile, const GemmArgs& a) {
+  float h[64];
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t v[64];
-    tmem_ld_4x16(taddr, 64 * half, 64 * half + 16, 64 * half + 32, 64 * half + 48, v);
-    float h[64];
+  for (int i = 0; i < 64; ++i) h[i] = relu_sq(lane_value(v[i], store));
+  if constexpr (FMT == kFmtNVFP4) {
+    uint32_t c[8];
+    uint32_t sf4 = 0;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) h[i] = relu_sq(lane_value(v[i], store));
-    if constexpr (FMT == kFmtNVFP4) {
+    for (int jb = 0; jb < 4; ++jb) {
+      uint8_t sf;
+      quant_nvfp4_16(h + 16 * jb, *reinterpret_cast<uint32_t(*)[2]>(&c[2 * jb]), sf);
+      sf4 |= static_cast<uint32_t>(sf) << (8 * jb);
+    }
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + p * 32);
+      dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+      dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+      *reinterpret_cast<uint32_t*>(
+          a.out_sf + sf_tile_offset(prow, n_tile * 8 + p * 4, a.out_sf_tiles_k)) = sf4;
+    }
+  } else if constexpr (FMT == kFmtMXFP8) {
+#pragma unroll
+    for (int jb = 0; jb < 2; ++jb) {
       uint32_t c[8];
-      uint32_t sf4 = 0;
-#pragma unroll
-      for (int jb = 0; jb < 4; ++jb) {
-        uint8_t sf;
-        quant_nvfp4_16(h + 16 * jb, *reinterpret_cast<uint32_t(*)[2]>(&c[2 * jb]), sf);
-        sf4 |= static_cast<uint32_t>(sf) << (8 * jb);
-      }
+      uint8_t sf;
+      quant_mxfp8_32(h + 32 * jb, c, sf);
       if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + half * 32);
+        uint4* dst =
+            reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 128 + p * 64 + jb * 32);
         dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
         dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-        *reinterpret_cast<uint32_t*>(
-            a.out_sf + sf_tile_offset(prow, n_tile * 8 + half * 4, a.out_sf_tiles_k)) = sf4;
+        a.out_sf[sf_tile_offset(prow, n_tile * 4 + p * 2 + jb, a.out_sf_tiles_k)] = sf;
       }
-    } else if constexpr (FMT == kFmtMXFP8) {
+    }
+  } else {
+    if (store) {
+      uint8_t* dst = a.out + prow * a.out_ld + (n_tile * 128 + p * 64) * 2;
 #pragma unroll
-      for (int jb = 0; jb < 2; ++jb) {
-        uint32_t c[8];
-        uint8_t sf;
-        quant_mxfp8_32(h + 32 * jb, c, sf);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 128 +
-                                                half * 64 + jb * 32);
-          dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-          dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-          a.out_sf[sf_tile_offset(prow, n_tile * 4 + half * 2 + jb, a.out_sf_tiles_k)] = sf;
-        }
-      }
-    } else {
-      if (store) {
-        uint8_t* dst = a.out + prow * a.out_ld + (n_tile * 128 + half * 64) * 2;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) store_bf16x16(dst + 32 * q, h + 16 * q);
-      }
+      for (int q = 0; q < 4; ++q) store_bf16x16(dst + 32 * q, h + 16 * q);
     }
   }
 }
 
-// GEMM2: 128 output features per row, stored as bf16; 64 columns per TMEM
-// wait.
-__device__ __forceinline__ void epilogue_gemm2(uint32_t taddr, bool store, int64_t prow,
+// GEMM2, round p: output features 128*n_tile + 64p + j, stored as bf16.
+__device__ __forceinline__ void epilogue_gemm2(const uint32_t* v, int p, bool store, int64_t prow,
                                                int n_tile, const GemmArgs& a) {
+  if (!store) return;
+  uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 256 + p * 128);
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t v[64];
-    tmem_ld_4x16(taddr, 64 * half, 64 * half + 16, 64 * half + 32, 64 * half + 48, v);
-    if (store) {
-      uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + (n_tile * 128 + half * 64) * 2);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                            pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                            pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                            pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
-    }
-  }
+  for (int q = 0; q < 8; ++q)
+    dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+}
+
+template <int FMT, int EPI>
+__device__ __forceinline__ void epilogue_round(const uint32_t* v, int p, bool store, int64_t prow,
+                                               int64_t orow, int n_tile, const GemmArgs& a) {
+  if constexpr (EPI == 1) epilogue_gemm1<FMT>(v, p, store, prow, n_tile, a);
+  else if constexpr (EPI == 3) epilogue_relu2<FMT>(v, p, store, prow, n_tile, a);
+  else epilogue_gemm2(v, p, store, orow, n_tile, a);
 }
 
 // ---------------------------------------------------------------- kernel
 template <int FMT, int EPI, int MROWS, int NW>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(NW), 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   constexpr int SFT = Fmt<FMT>::kSfTiles;
   constexpr int SB = stage_bytes<FMT, MROWS, NW>();
@@ -329,7 +331,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drained = tempty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 1);
+  uint64_t* sf_ready = drained + 1;  // [kStages] scales of the stage are in TMEM
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sf_ready + kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_tab = reinterpret_cast<int*>(tmem_holder + 4);
   const Tables tab{s_tab, s_tab + (args.E + 1), s_tab + (2 * args.E + 1)};
@@ -340,10 +343,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], 4 * NW);  // every epilogue warp releases the accumulator
     }
     mbar_init(drained, 1);
     *abort_flag = 0;
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
-  if (threadIdx.x == 32 * 2)
+  if (threadIdx.x == 32 * 2 + 1)
     for (int i = 0; i < 4; ++i) prefetch_tmap(&maps.a[i]);
   // Everything below reads what the previous kernels wrote.
   pdl_wait();
@@ -367,8 +371,74 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const int total = tab.chunk_off[args.E] * args.n_tiles;
+  // Decode launches: a chunk of at most 32 rows keeps all its real
+  // accumulator rows in TMEM lane quarter 0, and the MMA of each lane quarter
+  // reads both operands' scales from that quarter's own lanes, so such a
+  // chunk needs its stage's scales in lanes 0-31 only.  Warp 0 (the quarter-0
+  // warp) writes just those lanes from shared memory with tcgen05.st (4 KiB
+  // per stage instead of the 16 KiB a broadcast tcgen05.cp writes), off the
+  // tensor pipe; every stage of such a launch then reaches the MMA through
+  // warp 0's sf_ready barrier.
+  const bool staged = NW == 1 && SFT > 0 && args.pair_scale_copies && args.stage_scales;
 
   if (warp == 0) {
+    // ------------------------------------------------ scale stager
+    if (staged) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const bool q0 = map_item(tab, args.E, args.n_tiles, item).rows <= 32;
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          const bool landed = mbar_wait(&full[stage], phase, abort_flag);
+          if (!__all_sync(0xFFFFFFFFu, landed)) {
+            ok = false;
+            break;
+          }
+          if (q0) {
+            const uint8_t* sp = smem + stage * SB;
+            const uint32_t col = tmem + kSfColBase + stage * kSfColsPerStage;  // lanes 0-31
+            if constexpr (FMT == kFmtNVFP4) {
+              // per 64-element substep j: activation row (lane) scales in
+              // column 8j, the 128 weight rows' scales in columns 8j+4..8j+7
+              uint32_t v[32];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint4 b = *reinterpret_cast<const uint4*>(sp + kOffBsf + j * 512 + lane * 16);
+                v[8 * j] = *reinterpret_cast<const uint32_t*>(sp + kOffAsf + j * 512 + lane * 16);
+                v[8 * j + 1] = v[8 * j + 2] = v[8 * j + 3] = 0u;
+                v[8 * j + 4] = b.x;
+                v[8 * j + 5] = b.y;
+                v[8 * j + 6] = b.z;
+                v[8 * j + 7] = b.w;
+              }
+              tmem_st32(col, v);
+            } else {
+              // weight rows' scales in columns 0-3, activation row in 4
+              uint32_t v[8];
+              const uint4 b = *reinterpret_cast<const uint4*>(sp + kOffBsf + lane * 16);
+              v[0] = b.x;
+              v[1] = b.y;
+              v[2] = b.z;
+              v[3] = b.w;
+              v[4] = *reinterpret_cast<const uint32_t*>(sp + kOffAsf + lane * 16);
+              v[5] = v[6] = v[7] = 0u;
+              tmem_st8(col, v);
+            }
+            tmem_st_wait();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sf_ready[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && lane == 0) report_status(args.status, kStatusTimeout);
+    }
+  } else if (warp == 2) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t policy = l2_policy_evict_first();
@@ -462,7 +532,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * kAccCols;
         for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          if (!mbar_wait(staged ? &sf_ready[stage] : &full[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -491,7 +561,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
                        idesc_mxf8(128, 256, j), sf_col + 8, sf_col, (kb | j) != 0);
           } else if constexpr (FMT == kFmtNVFP4) {
-            if (q0_only) {
+            if (q0_only && staged) {
+              // lanes 0-31 of the stage's scale columns were written by warp 0
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                         sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
+            } else if (q0_only) {
               // columns: A scales of substeps 0-1 | 2-3, B scales 0-1 | 2-3
               const uint32_t sfa = smem_u32(sf + 4 * 512), sfb = smem_u32(sf);
               tc_copy_128x256b(sf_col, desc_sf_pair(sfa, 512));
@@ -516,7 +592,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                          sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
             }
           } else if constexpr (FMT == kFmtMXFP8) {
-            if (q0_only) {
+            if (q0_only && staged) {
+              // lanes 0-31 of the stage's scale columns were written by warp 0
+            } else if (q0_only) {
               // columns 0-3: B scales, 4-7: A scales (tiles adjacent in smem)
               tc_copy_128x256b(sf_col, desc_sf_pair(smem_u32(sf), 512));
             } else {
@@ -547,8 +625,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) report_status(args.status, kStatusTimeout);
     }
   } else {
-    // ------------------------------------------------ epilogue warps 2..5
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // ------------------------------------------------ epilogue warps 3..
+    // Warp w reads TMEM lane quarter w % 4 (rows 32q..) of accumulator
+    // column group (w - 3) / 4 (one 128-column group per weight tile).
+    const int q = warp & 3;
+    const int grp = (warp - 3) >> 2;
     int local = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++local) {
       const Item it = map_item(tab, args.E, args.n_tiles, item);
@@ -560,26 +641,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_after();
       const int r = q * 32 + lane;
-      if (q * 32 < it.rows) {
-        const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols;
-        const int64_t prow = it.prow0 + r;
-        // batched format: expert e's rows go to rows e*M.. of the output
-        const int64_t orow = args.out_rows_per_expert
-                                 ? static_cast<int64_t>(it.e) * args.out_rows_per_expert +
-                                       (it.prow0 - tab.pad_off[it.e]) + r
-                                 : prow;
+      const bool active = q * 32 < it.rows;
+      const uint32_t taddr =
+          tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols + grp * 128;
+      const int64_t prow = it.prow0 + r;
+      // batched format: expert e's rows go to rows e*M.. of the output
+      const int64_t orow = args.out_rows_per_expert
+                               ? static_cast<int64_t>(it.e) * args.out_rows_per_expert +
+                                     (it.prow0 - tab.pad_off[it.e]) + r
+                               : prow;
+      const int n128 = it.n_tile * NW + grp;
+      if constexpr (NW == 1) {
+        if (active) {
 #pragma unroll
-        for (int g = 0; g < NW; ++g) {  // one 128-column group per weight tile
-          const uint32_t taddr = tbase + g * 128;
-          const int n128 = it.n_tile * NW + g;
-          if constexpr (EPI == 1) epilogue_gemm1<FMT>(taddr, r < it.rows, prow, n128, args);
-          else if constexpr (EPI == 3) epilogue_relu2<FMT>(taddr, r < it.rows, prow, n128, args);
-          else epilogue_gemm2(taddr, r < it.rows, orow, n128, args);
+          for (int p = 0; p < 2; ++p) {
+            uint32_t v[64];
+            epilogue_load<EPI>(taddr, p, v);
+            tmem_ld_wait();
+            epilogue_fence(v);
+            epilogue_round<FMT, EPI>(v, p, r < it.rows, prow, orow, n128, args);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+      } else {
+        uint32_t v[128];
+        if (active) {
+          epilogue_load<EPI>(taddr, 0, v);
+          epilogue_load<EPI>(taddr, 1, v + 64);
+          tmem_ld_wait();
+          epilogue_fence(v);
+          epilogue_fence(v + 64);
+        }
+        // the accumulator is free for the next item's MMAs from here on
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (active) {
+          epilogue_round<FMT, EPI>(v, 0, r < it.rows, prow, orow, n128, args);
+          epilogue_round<FMT, EPI>(v + 64, 1, r < it.rows, prow, orow, n128, args);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
     }
   }
 
@@ -592,7 +695,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <int FMT, int EPI, int MROWS, int NW>
 cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t s) {
   return launch_pdl(g_pdl_gemm, moe_gemm_kernel<FMT, EPI, MROWS, NW>, dim3(grid),
-                    dim3(kGemmThreads), smem_bytes<FMT, MROWS, NW>(), s, maps, args);
+                    dim3(gemm_threads(NW)), smem_bytes<FMT, MROWS, NW>(), s, maps, args);
 }
 
 template <int FMT, int EPI, int MROWS, int NW>

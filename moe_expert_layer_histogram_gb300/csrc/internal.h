@@ -14,7 +14,6 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 constexpr int kTokensPerRouteBlock = 8;   // tokens per routing/scatter block (warp each)
 constexpr int kRowBlock = 128;            // expert segments padded to this
-constexpr int kGemmThreads = 192;         // producer, MMA, 4 epilogue warps
 
 // Device status word codes (read back by moe_get_status).
 constexpr int kStatusBadCount = 1;  // MOE_ERR_INVALID_ARG: a batched count outside [0, M]
@@ -46,7 +45,8 @@ struct GemmArgs {
   uint8_t* out_sf;           // GEMM1 (MX/NV): GEMM2 input scales
   int out_sf_tiles_k;
   float clamp;               // +inf: no clamp
-  int pair_scale_copies;     // 1: chunks of <= 32 rows copy scales to lanes 0-31 only
+  int pair_scale_copies;     // 1: chunks of <= 32 rows need scales in lanes 0-31 only
+  int stage_scales;          // 1: ... which a dedicated warp writes there (tcgen05.st)
   int out_rows_per_expert;   // 0: output row = padded row; M > 0 (batched format):
                              // output row = e * M + row within the expert
   int* status;

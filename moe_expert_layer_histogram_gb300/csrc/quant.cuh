@@ -61,21 +61,33 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float* q) {
 // ---------------------------------------------------------------- blocks
 // x[16] -> codes[2] (8 bytes, element 2j in the low nibble) and one e4m3
 // scale byte.
+// Zero dividends are answered without dividing (the quotient is the signed
+// zero itself): the correctly rounded divide is much slower on them, and a
+// squared-ReLU block is half zeros.  Blocks without zeros keep sixteen
+// independent divides (a select around each one costs their overlap).
 __device__ __forceinline__ void quant_nvfp4_16(const float* x, uint32_t (&codes)[2],
                                                uint8_t& sf) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const uint8_t c = float_to_e4m3(__fdiv_rn(amax, 6.0f));
+  const uint8_t c = amax == 0.0f ? uint8_t{0} : float_to_e4m3(__fdiv_rn(amax, 6.0f));
   const float sv = e4m3_to_float(c);
   sf = c;
   if (sv == 0.0f) {
     codes[0] = codes[1] = 0u;
     return;
   }
-  float q[16];
+  bool has_zero = false;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(x[i], sv);
+  for (int i = 0; i < 16; ++i) has_zero |= x[i] == 0.0f;
+  float q[16];
+  if (!has_zero) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(x[i], sv);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = x[i] == 0.0f ? x[i] : __fdiv_rn(x[i], sv);
+  }
   codes[0] = cvt_e2m1x8(q);
   codes[1] = cvt_e2m1x8(q + 8);
 }
