@@ -189,8 +189,10 @@ moe_status moe_get_status(moe_layer *layer);
  * max_forwards forwards; the events are created here, not in the forward.
  * moe_timing_stop waits for the recorded work, writes the summed duration
  * of each kernel in milliseconds to kernel_ms[6] (routing, scan, scatter +
- * activation quantisation, GEMM1 + SwiGLU, GEMM2, combine) and the number of
- * recorded forwards to *forwards, and turns timing off.  Errors:
+ * activation quantisation, GEMM1 + SwiGLU, GEMM2, combine; for T <= 16 one
+ * kernel does routing .. quantisation and is counted as routing, scan and
+ * scatter reading 0) and the number of recorded forwards to *forwards, and
+ * turns timing off.  Errors:
  * MOE_ERR_INVALID_ARG, MOE_ERR_CUDA.                                       */
 moe_status moe_timing_start(moe_layer *layer, int max_forwards);
 moe_status moe_timing_stop(moe_layer *layer, float *kernel_ms, int *forwards);

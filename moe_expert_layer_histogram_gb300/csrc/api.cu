@@ -372,13 +372,27 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     if (ev) cudaEventRecord(ev[i], s);
   };
   mark(0);
-  cudaError_t e = launch_route(logits, T, E, K, L->ids, L->w, L->blockhist, s);
-  mark(1);
-  if (e == cudaSuccess) e = launch_expert_scan(L->blockhist, NB, E, L->prefix, L->counts, s);
-  mark(2);
-  if (e == cudaSuccess)
-    e = launch_scatter_quant(L->fmt, L->ids, T, E, K, hidden, H, L->prefix, L->counts, L->offsets,
-                             L->pad_off, L->chunk_off, L->perm, L->inv, L->xq, L->xsf, s);
+  cudaError_t e;
+  int launches = 4;
+  const bool small = T <= kSmallFrontTokens;
+  if (small) {
+    // one kernel for routing .. GEMM1 input (timed as the routing kernel)
+    e = launch_small_front(L->fmt, logits, T, E, K, hidden, H, L->ids, L->w, L->counts,
+                           L->offsets, L->pad_off, L->chunk_off, L->perm, L->inv, L->xq, L->xsf,
+                           s);
+    mark(1);
+    mark(2);
+  } else {
+    e = launch_route(logits, T, E, K, L->ids, L->w, L->blockhist, s);
+    mark(1);
+    if (e == cudaSuccess) e = launch_expert_scan(L->blockhist, NB, E, L->prefix, L->counts, s);
+    mark(2);
+    if (e == cudaSuccess)
+      e = launch_scatter_quant(L->fmt, L->ids, T, E, K, hidden, H, L->prefix, L->counts,
+                               L->offsets, L->pad_off, L->chunk_off, L->perm, L->inv, L->xq,
+                               L->xsf, s);
+    launches = 6;
+  }
   mark(3);
   const int64_t chunks = max_chunks(L, T);
   const int pair = L->pair_scale_copies && T <= kPairCopyMaxTokens;
@@ -391,7 +405,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   mark(6);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   L->last_T = T;
-  L->last_launches = 6;
+  L->last_launches = launches;
   return MOE_OK;
 }
 

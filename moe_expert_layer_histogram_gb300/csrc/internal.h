@@ -13,6 +13,7 @@ constexpr int kFmtBF16 = 0, kFmtMXFP8 = 1, kFmtNVFP4 = 2;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 constexpr int kTokensPerRouteBlock = 8;   // tokens per routing/scatter block (warp each)
+constexpr int kSmallFrontTokens = 16;     // up to this T one block does routing..quantisation
 constexpr int kRowBlock = 128;            // expert segments padded to this
 
 // Device status word codes (read back by moe_get_status).
@@ -120,6 +121,12 @@ cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int 
                                  uint8_t* xsf, cudaStream_t s);
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int K, int H,
                            void* out, cudaStream_t s);
+// T <= kSmallFrontTokens: routing, scans, ranks and GEMM1 input in one block.
+cudaError_t launch_small_front(int fmt, const float* logits, int T, int E, int K,
+                               const void* hidden, int H, int32_t* ids, float* w,
+                               int32_t* counts, int32_t* offsets, int32_t* pad_off,
+                               int32_t* chunk_off, int32_t* perm, int32_t* inv, uint8_t* xq,
+                               uint8_t* xsf, cudaStream_t s);
 // Batched-expert format: per-expert tables from the counts and the GEMM1
 // input rows of hidden [E, M, H].
 cudaError_t launch_batched_quant(int fmt, const void* hidden, const int32_t* counts_in, int M,

@@ -43,53 +43,61 @@ __device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float (&f)[N])
   }
 }
 
-// One warp writes the GEMM1 input of one token row x [H] into the padded
-// rows prows[0..n): BF16 copied, MXFP8 / NVFP4 quantised per block (lane l
-// takes blocks l, l+32, ...), codes row-major and scales in the MMA's
-// 128-row scale tiles.
+// Units of one token row's GEMM1 input: 16-byte chunks (BF16, copied) or
+// quantisation blocks of 16 (NVFP4) / 32 (MXFP8) elements.
+template <int FMT>
+__host__ __device__ constexpr int row_units(int H) {
+  return FMT == kFmtBF16 ? H / 8 : FMT == kFmtNVFP4 ? H / 16 : H / 32;
+}
+
+// Unit `u` of token row x [H] into the padded rows prows[0..n): BF16 copied,
+// MXFP8 / NVFP4 quantised, codes row-major and scales in the MMA's 128-row
+// scale tiles.
+template <int FMT>
+__device__ __forceinline__ void quant_unit_to_rows(const __nv_bfloat16* __restrict__ x, int H,
+                                                   int u, const int* prows, int n,
+                                                   uint8_t* __restrict__ xq,
+                                                   uint8_t* __restrict__ xsf) {
+  if constexpr (FMT == kFmtBF16) {
+    const uint4 val = reinterpret_cast<const uint4*>(x)[u];
+    for (int k = 0; k < n; ++k)
+      reinterpret_cast<uint4*>(xq + static_cast<int64_t>(prows[k]) * H * 2)[u] = val;
+  } else if constexpr (FMT == kFmtNVFP4) {
+    float f[16];
+    load_bf16<16>(x + u * 16, f);
+    uint32_t codes[2];
+    uint8_t sf;
+    quant_nvfp4_16(f, codes, sf);
+    for (int k = 0; k < n; ++k) {
+      const int64_t prow = prows[k];
+      *reinterpret_cast<uint2*>(xq + prow * (H / 2) + u * 8) = make_uint2(codes[0], codes[1]);
+      xsf[sf_tile_offset(prow, u, H / 64)] = sf;
+    }
+  } else {
+    float f[32];
+    load_bf16<32>(x + u * 32, f);
+    uint32_t codes[8];
+    uint8_t sf;
+    quant_mxfp8_32(f, codes, sf);
+    for (int k = 0; k < n; ++k) {
+      const int64_t prow = prows[k];
+      uint4* dst = reinterpret_cast<uint4*>(xq + prow * H + u * 32);
+      dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      xsf[sf_tile_offset(prow, u, H / 128)] = sf;
+    }
+  }
+}
+
+// One warp writes the GEMM1 input of one token row into its padded rows
+// (lane l takes units l, l+32, ...).
 template <int FMT>
 __device__ __forceinline__ void quant_row_to_rows(const __nv_bfloat16* __restrict__ x, int H,
                                                   const int* prows, int n,
                                                   uint8_t* __restrict__ xq,
                                                   uint8_t* __restrict__ xsf, int lane) {
-  if constexpr (FMT == kFmtBF16) {
-    const uint4* src = reinterpret_cast<const uint4*>(x);
-    for (int c = lane; c < H / 8; c += 32) {
-      const uint4 val = src[c];
-      for (int k = 0; k < n; ++k)
-        reinterpret_cast<uint4*>(xq + static_cast<int64_t>(prows[k]) * H * 2)[c] = val;
-    }
-  } else if constexpr (FMT == kFmtNVFP4) {
-    const int tiles_k = H / 64;
-    for (int blk = lane; blk < H / 16; blk += 32) {
-      float f[16];
-      load_bf16<16>(x + blk * 16, f);
-      uint32_t codes[2];
-      uint8_t sf;
-      quant_nvfp4_16(f, codes, sf);
-      for (int k = 0; k < n; ++k) {
-        const int64_t prow = prows[k];
-        *reinterpret_cast<uint2*>(xq + prow * (H / 2) + blk * 8) = make_uint2(codes[0], codes[1]);
-        xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
-      }
-    }
-  } else {
-    const int tiles_k = H / 128;
-    for (int blk = lane; blk < H / 32; blk += 32) {
-      float f[32];
-      load_bf16<32>(x + blk * 32, f);
-      uint32_t codes[8];
-      uint8_t sf;
-      quant_mxfp8_32(f, codes, sf);
-      for (int k = 0; k < n; ++k) {
-        const int64_t prow = prows[k];
-        uint4* dst = reinterpret_cast<uint4*>(xq + prow * H + blk * 32);
-        dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-        dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-        xsf[sf_tile_offset(prow, blk, tiles_k)] = sf;
-      }
-    }
-  }
+  for (int u = lane; u < row_units<FMT>(H); u += 32)
+    quant_unit_to_rows<FMT>(x, H, u, prows, n, xq, xsf);
 }
 
 // ---------------------------------------------------------------- routing
@@ -97,21 +105,14 @@ __device__ __forceinline__ void quant_row_to_rows(const __nv_bfloat16* __restric
 // K rounds of a warp arg-max in the total order (value descending, index
 // ascending), then the softmax of the K selected values.  Block b also counts
 // how many of its slots go to each expert (blockhist[b][e]).
+// One warp routes the token with logits l[E]: lane k < K receives the k-th
+// expert in *id and its softmax weight in *wt.
 template <int MAXJ>
-__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E,
-                                                    int K, int32_t* __restrict__ ids,
-                                                    float* __restrict__ w,
-                                                    int32_t* __restrict__ blockhist) {
-  pdl_launch_dependents();
-  __shared__ int hist[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kTokensPerRouteBlock + warp;
-  float my_v = 0.0f, ex = 0.0f, sum = 1.0f;
+__device__ __forceinline__ void route_token(const float* __restrict__ l, int E, int K, int lane,
+                                            int* id, float* wt) {
+  float my_v = 0.0f;
   int my_i = 0;
-  if (t < T) {
-    const float* l = logits + static_cast<int64_t>(t) * E;
+  {
     float v[MAXJ];
     uint32_t avail = 0;
 #pragma unroll
@@ -148,17 +149,35 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
         my_i = bi;
       }
     }
-    const float m = __shfl_sync(kFull, my_v, 0);
-    ex = lane < K ? expf(my_v - m) : 0.0f;
-    sum = ex;
-#pragma unroll
-    for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
   }
+  const float m = __shfl_sync(kFull, my_v, 0);
+  const float ex = lane < K ? expf(my_v - m) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+  *id = my_i;
+  *wt = ex / sum;
+}
+
+template <int MAXJ>
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E,
+                                                    int K, int32_t* __restrict__ ids,
+                                                    float* __restrict__ w,
+                                                    int32_t* __restrict__ blockhist) {
+  pdl_launch_dependents();
+  __shared__ int hist[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTokensPerRouteBlock + warp;
+  int my_i = 0;
+  float my_w = 0.0f;
+  if (t < T) route_token<MAXJ>(logits + static_cast<int64_t>(t) * E, E, K, lane, &my_i, &my_w);
   // the previous forward's last kernels may still read ids / w / blockhist
   pdl_wait();
   if (t < T && lane < K) {
     ids[static_cast<int64_t>(t) * K + lane] = my_i;
-    w[static_cast<int64_t>(t) * K + lane] = ex / sum;
+    w[static_cast<int64_t>(t) * K + lane] = my_w;
     atomicAdd(&hist[my_i], 1);
   }
   __syncthreads();
@@ -301,6 +320,111 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
   if (warp >= ntok) return;
   quant_row_to_rows<FMT>(hidden + static_cast<int64_t>(tok0 + warp) * H, H, s_prow + warp * K, K,
                          xq, xsf, lane);
+}
+
+// ---------------------------------------------------------------- small batches
+// Decode batches (T <= kSmallFrontTokens): routing, the expert histogram and
+// scans, the stable ranks and the GEMM1 input in one kernel, in place of the
+// three kernels above (each of which would otherwise wait for the previous
+// one).  One block per token: every block routes all T tokens and derives
+// the same tables (a few microseconds of redundant work), block 0 stores
+// them, and block b spreads token b's input quantisation over its 256
+// threads instead of one warp.
+template <int FMT, int MAXJ>
+__global__ void __launch_bounds__(256) small_front_kernel(
+    const float* __restrict__ logits, int T, int E, int K, const __nv_bfloat16* __restrict__ hidden,
+    int H, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ pad_off, int32_t* __restrict__ chunk_off,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, uint8_t* __restrict__ xq,
+    uint8_t* __restrict__ xsf) {
+  pdl_launch_dependents();
+  __shared__ int hist[kMaxExperts], cnt[kMaxExperts], s_off[kMaxExperts], s_poff[kMaxExperts];
+  __shared__ int s_ids[kSmallFrontTokens * kMaxTopK], s_prow[kSmallFrontTokens * kMaxTopK];
+  __shared__ int wsum[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = cnt[e] = 0;
+  __syncthreads();
+  // the previous forward's last kernels may still read what this one writes
+  pdl_wait();
+
+  const bool store = blockIdx.x == 0;
+  // 1. routing: warp w takes tokens w, w + 8
+  for (int t = warp; t < T; t += 8) {
+    int my_i;
+    float my_w;
+    route_token<MAXJ>(logits + static_cast<int64_t>(t) * E, E, K, lane, &my_i, &my_w);
+    if (lane < K) {
+      if (store) {
+        ids[t * K + lane] = my_i;
+        w[t * K + lane] = my_w;
+      }
+      s_ids[t * K + lane] = my_i;
+      atomicAdd(&hist[my_i], 1);
+    }
+  }
+  __syncthreads();
+
+  // 2. per-expert offsets (two experts per thread, E <= 512)
+  const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
+  const int c0 = e0 < E ? hist[e0] : 0, c1 = e1 < E ? hist[e1] : 0;
+  const int p0 = (c0 + kRowBlock - 1) / kRowBlock, p1 = (c1 + kRowBlock - 1) / kRowBlock;
+  const int xo = block_scan_pair(c0 + c1, wsum);
+  const int xp = block_scan_pair((p0 + p1) * kRowBlock, wsum);
+  const int xc = block_scan_pair(p0 + p1, wsum);
+  if (e0 < E) {
+    s_off[e0] = xo;
+    s_poff[e0] = xp;
+  }
+  if (e1 < E) {
+    s_off[e1] = xo + c0;
+    s_poff[e1] = xp + p0 * kRowBlock;
+  }
+  if (store) {
+    if (e0 < E) {
+      counts[e0] = c0;
+      offsets[e0] = xo;
+      pad_off[e0] = xp;
+      chunk_off[e0] = xc;
+    }
+    if (e1 < E) {
+      counts[e1] = c1;
+      offsets[e1] = xo + c0;
+      pad_off[e1] = xp + p0 * kRowBlock;
+      chunk_off[e1] = xc + p0;
+    }
+    if (e0 == E - 1 || e1 == E - 1) {
+      offsets[E] = xo + c0 + c1;
+      pad_off[E] = xp + (p0 + p1) * kRowBlock;
+      chunk_off[E] = xc + p0 + p1;
+    }
+  }
+  __syncthreads();
+
+  // 3. stable ranks in slot order s = t*K + k (the K experts of a token
+  //    are distinct, so one token's slots never share a counter)
+  if (warp == 0) {
+    for (int t = 0; t < T; ++t) {
+      if (lane < K) {
+        const int s = t * K + lane;
+        const int e = s_ids[s];
+        const int r = cnt[e]++;
+        const int prow = s_poff[e] + r;
+        if (store) {
+          perm[s_off[e] + r] = s;
+          inv[s] = prow;
+        }
+        s_prow[s] = prow;
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
+  // 4. token b's GEMM1 input rows, its units spread over the block
+  const int t = blockIdx.x;
+  for (int u = threadIdx.x; u < row_units<FMT>(H); u += blockDim.x)
+    quant_unit_to_rows<FMT>(hidden + static_cast<int64_t>(t) * H, H, u, s_prow + t * K, K, xq,
+                            xsf);
 }
 
 // ---------------------------------------------------------------- batched format
@@ -489,6 +613,26 @@ cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int 
            : fmt == kFmtMXFP8 ? scatter_quant_kernel<kFmtMXFP8>
                               : scatter_quant_kernel<kFmtNVFP4>;
   return launch_pdl(g_pdl_small, k, dim3(nb), dim3(256), 0, s, ids, T, E, K, hb, H, prefix,
+                    counts, offsets, pad_off, chunk_off, perm, inv, xq, xsf);
+}
+
+cudaError_t launch_small_front(int fmt, const float* logits, int T, int E, int K,
+                               const void* hidden, int H, int32_t* ids, float* w,
+                               int32_t* counts, int32_t* offsets, int32_t* pad_off,
+                               int32_t* chunk_off, int32_t* perm, int32_t* inv, uint8_t* xq,
+                               uint8_t* xsf, cudaStream_t s) {
+  if (T > kSmallFrontTokens) return cudaErrorInvalidValue;
+  const auto* hb = static_cast<const __nv_bfloat16*>(hidden);
+  auto pick = [&](auto k4, auto k8, auto k16) { return E <= 128 ? k4 : E <= 256 ? k8 : k16; };
+  auto k = fmt == kFmtBF16
+               ? pick(small_front_kernel<kFmtBF16, 4>, small_front_kernel<kFmtBF16, 8>,
+                      small_front_kernel<kFmtBF16, 16>)
+           : fmt == kFmtMXFP8
+               ? pick(small_front_kernel<kFmtMXFP8, 4>, small_front_kernel<kFmtMXFP8, 8>,
+                      small_front_kernel<kFmtMXFP8, 16>)
+               : pick(small_front_kernel<kFmtNVFP4, 4>, small_front_kernel<kFmtNVFP4, 8>,
+                      small_front_kernel<kFmtNVFP4, 16>);
+  return launch_pdl(g_pdl_small, k, dim3(T), dim3(256), 0, s, logits, T, E, K, hb, H, ids, w,
                     counts, offsets, pad_off, chunk_off, perm, inv, xq, xsf);
 }
 

@@ -26,6 +26,10 @@ CASES = [
     ("bf16_small", dict(T=300, E=4, K=2)),          # >128 rows per expert: several chunks
     ("nvfp4_small", dict(T=200, E=3, K=2)),
     ("mxfp8_small", dict(T=180, E=3, K=1)),
+    # T <= 16: the one-block front end (routing .. GEMM1 input in one kernel)
+    ("nvfp4_small", dict(T=5, E=300, K=8)),
+    ("mxfp8_small", dict(T=16, E=200, K=6)),
+    ("bf16_small", dict(T=9, E=40, K=3)),
 ]
 
 
