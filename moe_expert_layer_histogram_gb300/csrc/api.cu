@@ -50,6 +50,7 @@ struct moe_layer {
   int pair_scale_copies = 1;
   int wide_tiles = -1;               // 0 off, 1 always, -1 for prefill-sized launches
   int stage_scales = 1;              // decode scales written by a warp, not copied
+  int test_stall = 0;                // test hook (MOE_TEST_STALL_GEMM): GEMM1 times out
   bool weights_ready = false;
   int last_T = 0, last_launches = 0;
   std::vector<cudaEvent_t> tev;  // per-kernel timing events, 7 per forward
@@ -156,6 +157,7 @@ cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
   a.clamp = L->clamp;
   a.pair_scale_copies = pair;
   a.stage_scales = L->stage_scales;
+  a.test_stall = L->test_stall;
   a.out_rows_per_expert = 0;
   a.status = L->status;
   const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
@@ -278,6 +280,10 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   // MOE_SCALE_STAGER=0: decode chunks copy their scales with tcgen05.cp
   // (lanes 0-31 through 128x256b copies) instead of a staging warp.
   if (const char* sv = std::getenv("MOE_SCALE_STAGER")) L->stage_scales = sv[0] != '0';
+  // Test hook for the bounded waits: MOE_TEST_STALL_GEMM=1 makes one CTA of
+  // every GEMM1 launch leave one stage unloaded; its waits give up after
+  // 2 s and moe_get_status reports MOE_ERR_DEVICE_TIMEOUT.
+  if (const char* tv = std::getenv("MOE_TEST_STALL_GEMM")) L->test_stall = tv[0] == '1';
   const int H = L->H, I = L->I, E = L->E;
   if (L->fmt == MOE_FMT_NVFP4) {
     L->xb = H / 2; L->hb = I / 2; L->x_tiles_k = H / 64; L->h_tiles_k = I / 64;

@@ -444,7 +444,8 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
       const uint64_t policy = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
-      int issued = 0;
+      int slots = 0;          // ring positions used so far
+      int skipped = -1;       // position the test hook left unloaded
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const Item it = map_item(tab, args.E, args.n_tiles, item);
@@ -464,6 +465,15 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
+          }
+          if (args.test_stall && blockIdx.x == 0 && skipped < 0) {
+            // test hook: nothing ever completes this stage
+            skipped = slots++;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
           }
           uint8_t* sp = smem + stage * SB;
           mbar_arrive_expect_tx(&full[stage], bytes);
@@ -487,7 +497,7 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
           }
           if constexpr (SFT > 0)
             bulk_load(sp + kOffAsf, sfa + kb * SFT * 512, SFT * 512, &full[stage]);
-          ++issued;
+          ++slots;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -496,8 +506,9 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
       }
       // Before leaving, make sure no copy this thread issued is still in
       // flight (they all completed already unless the block gave up).
-      for (int back = 1; back <= kStages && back <= issued; ++back) {
-        const int idx = issued - back;
+      for (int back = 1; back <= kStages && back <= slots; ++back) {
+        const int idx = slots - back;
+        if (idx == skipped) continue;
         mbar_wait(&full[idx % kStages], static_cast<uint32_t>((idx / kStages) & 1), nullptr);
       }
       if (!ok) report_status(args.status, kStatusTimeout);

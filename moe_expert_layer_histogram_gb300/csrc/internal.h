@@ -48,6 +48,8 @@ struct GemmArgs {
   float clamp;               // +inf: no clamp
   int pair_scale_copies;     // 1: chunks of <= 32 rows need scales in lanes 0-31 only
   int stage_scales;          // 1: ... which a dedicated warp writes there (tcgen05.st)
+  int test_stall;            // test hook: CTA 0 never loads one stage, so the waits on it
+                             // run out (bounded) and the kernel reports a timeout
   int out_rows_per_expert;   // 0: output row = padded row; M > 0 (batched format):
                              // output row = e * M + row within the expert
   int* status;

@@ -1,0 +1,44 @@
+"""Bounded device waits (GPU): a GEMM whose data never arrives gives up.
+
+The test hook MOE_TEST_STALL_GEMM=1 (read when a layer is created) makes one
+CTA of every GEMM1 launch leave one stage of its shared-memory ring unloaded,
+so the barrier waits on that stage are never satisfied.  Each wait gives up
+after 2 s: the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its own copies,
+frees its tensor memory and returns.  No fault, trap or hang is involved, and
+the CUDA context stays usable, which the second half checks.
+"""
+import time
+
+import numpy as np
+import pytest
+
+import workloads
+from tests.gpu_helpers import TOL, bf16_bits_to_f64, make_layer, rel_l2, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+MOE_ERR_DEVICE_TIMEOUT = 6
+
+
+def test_gemm_wait_runs_out_and_is_reported(monkeypatch):
+    s = workloads.spec("nvfp4_small")
+    case = workloads.make_case(s, seed=21)
+    monkeypatch.setenv("MOE_TEST_STALL_GEMM", "1")
+    layer = make_layer(s, weights=case["weights"])
+    t0 = time.perf_counter()
+    run_gpu(layer, case["hidden"], case["logits"])
+    waited = time.perf_counter() - t0
+    assert layer.status() == MOE_ERR_DEVICE_TIMEOUT
+    assert layer.status() == 0                      # read once, then cleared
+    assert 1.5 < waited < 60.0, waited
+    layer.close()
+
+    # the context is intact: a layer without the hook computes correctly
+    monkeypatch.delenv("MOE_TEST_STALL_GEMM")
+    layer = make_layer(s, weights=case["weights"])
+    out = run_gpu(layer, case["hidden"], case["logits"])
+    assert layer.status() == 0
+    ref = run_oracle(s, case)
+    assert rel_l2(out.float().cpu().numpy(), bf16_bits_to_f64(ref["out"])) <= TOL["nvfp4"]
+    assert np.isfinite(out.float().cpu().numpy()).all()
+    layer.close()
