@@ -45,6 +45,9 @@ def parse_args():
                    help="override E (small cases for profiler captures)")
     p.add_argument("--act", default="", choices=["", "swiglu", "relu2"],
                    help="expert activation (default: the workload's; relu2 drops the clamp)")
+    p.add_argument("--combine", default="gather", choices=["gather", "reduce"],
+                   help="sum of the K expert outputs: combine kernel (deterministic) or "
+                        "in-kernel atomic reduce")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -57,6 +60,7 @@ def workload_spec(args):
         s["T"] = args.tokens
     if args.experts:
         s["E"] = args.experts
+    s["combine"] = args.combine
     if args.act:
         s["act"] = args.act
         if args.act == "relu2":
@@ -65,9 +69,10 @@ def workload_spec(args):
 
 
 def describe(s):
-    return "%s: T=%d H=%d I=%d E=%d top-%d %s %s%s, logits %s" % (
+    return "%s: T=%d H=%d I=%d E=%d top-%d %s %s%s, logits %s%s" % (
         s["name"], s["T"], s["H"], s["I"], s["E"], s["K"], s["fmt"], s.get("act", "swiglu"),
-        (", clamp %g" % s["clamp"]) if s["clamp"] else "", s["logits"])
+        (", clamp %g" % s["clamp"]) if s["clamp"] else "", s["logits"],
+        ", in-kernel reduce" if s.get("combine") == "reduce" else "")
 
 
 def dtype_of(s):
@@ -228,7 +233,8 @@ def run_ours(args):
     T = s["T"]
 
     case = workloads.make_case(s, seed=0, device=dev)
-    layer = moe.MoELayer(T, s["H"], s["I"], s["E"], s["K"], s["fmt"], s["clamp"], s["act"])
+    layer = moe.MoELayer(T, s["H"], s["I"], s["E"], s["K"], s["fmt"], s["clamp"], s["act"],
+                         s["combine"])
     layer.prepare_weights(case["weights"])
     torch.cuda.synchronize()
     w_sample = None

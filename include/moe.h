@@ -73,6 +73,16 @@ typedef enum { MOE_FMT_BF16 = 0, MOE_FMT_MXFP8 = 1, MOE_FMT_NVFP4 = 2 } moe_form
  * item 4: models without a gated act-and-mul MLP, e.g. Nemotron).        */
 typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_RELU2 = 1 } moe_activation;
 
+/* How the K expert outputs of a token are summed.  GATHER (default): GEMM2
+ * stores each routed row's output as bf16 and a separate kernel sums the K
+ * rows of every token in k order (deterministic).  REDUCE: GEMM2's epilogue
+ * adds w * (fp32 output) into an fp32 accumulator with atomics and the last
+ * of a token's K contributions writes the bf16 result, so no combine kernel
+ * runs; the summation order, hence the last bits, can differ from run to
+ * run (the in-kernel reduce the MegaMoE kernel-drop workflow page, sec. 六,
+ * weighs against a deterministic combine).                                 */
+typedef enum { MOE_COMBINE_GATHER = 0, MOE_COMBINE_REDUCE = 1 } moe_combine;
+
 typedef struct {
     int max_tokens;    /* T_max: largest T any forward will use (>= 1)       */
     int hidden;        /* H: multiple of 128 (NVFP4: of 256)                 */
@@ -84,6 +94,7 @@ typedef struct {
                           before silu(gate)*up; otherwise no clamp (a clamp
                           with MOE_ACT_RELU2 is MOE_ERR_UNSUPPORTED)        */
     int activation;    /* moe_activation (0 = SwiGLU)                       */
+    int combine;       /* moe_combine (0 = gather)                          */
 } moe_config;
 
 typedef struct moe_layer moe_layer;   /* opaque */

@@ -17,6 +17,7 @@ LIB_PATH = _build.LIB
 
 MOE_FMT = {"bf16": 0, "mxfp8": 1, "nvfp4": 2}
 MOE_ACT = {"swiglu": 0, "relu2": 1}
+MOE_COMBINE = {"gather": 0, "reduce": 1}
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_NO_WEIGHTS", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_OOM",
@@ -27,7 +28,8 @@ class MoEConfig(ctypes.Structure):
     _fields_ = [("max_tokens", ctypes.c_int), ("hidden", ctypes.c_int),
                 ("inter", ctypes.c_int), ("num_experts", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("format", ctypes.c_int),
-                ("clamp_limit", ctypes.c_float), ("activation", ctypes.c_int)]
+                ("clamp_limit", ctypes.c_float), ("activation", ctypes.c_int),
+                ("combine", ctypes.c_int)]
 
 
 class MoEError(RuntimeError):
@@ -100,10 +102,11 @@ def moe_status_string(code):
 
 
 def moe_create(max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit=0.0,
-               activation="swiglu"):
+               activation="swiglu", combine="gather"):
     cfg = MoEConfig(int(max_tokens), int(hidden), int(inter), int(num_experts), int(top_k),
                     MOE_FMT[fmt] if isinstance(fmt, str) else int(fmt), float(clamp_limit or 0.0),
-                    MOE_ACT[activation] if isinstance(activation, str) else int(activation))
+                    MOE_ACT[activation] if isinstance(activation, str) else int(activation),
+                    MOE_COMBINE[combine] if isinstance(combine, str) else int(combine))
     h = ctypes.c_void_p()
     _check(lib().moe_create(ctypes.byref(cfg), ctypes.byref(h)), "moe_create")
     return h.value
@@ -199,14 +202,14 @@ class MoELayer:
     work goes on torch's current stream."""
 
     def __init__(self, max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit=0.0,
-                 activation="swiglu"):
+                 activation="swiglu", combine="gather"):
         import torch
         self.torch = torch
         self.H, self.I, self.E, self.K = hidden, inter, num_experts, top_k
         self.fmt = fmt
         self.max_tokens = max_tokens
         self.handle = moe_create(max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit,
-                                 activation)
+                                 activation, combine)
         self.T = 0
 
     def _stream(self):

@@ -40,6 +40,9 @@ struct moe_layer {
   int32_t *ids = nullptr, *blockhist = nullptr, *prefix = nullptr;
   int32_t *offsets = nullptr, *pad_off = nullptr, *chunk_off = nullptr, *counts = nullptr;
   int32_t *perm = nullptr, *inv = nullptr;
+  int combine = MOE_COMBINE_GATHER;
+  float* acc = nullptr;              // in-kernel reduce: fp32 [Tmax, H], zero between forwards
+  int32_t *acc_cnt = nullptr, *prow_slot = nullptr;
   float* w = nullptr;
   uint8_t *xq = nullptr, *xsf = nullptr, *hq = nullptr, *hsf = nullptr, *y = nullptr;
   uint8_t *w13t = nullptr, *w2t = nullptr;  // prepared weight tiles
@@ -167,8 +170,10 @@ cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
 
 // GEMM2 into `out` (bf16, H per row): padded rows (rows_per_expert 0) or
 // rows e*rows_per_expert + i (batched format).
+// reduce_out (routed forward with the in-kernel reduce): the bf16 layer
+// output, summed by GEMM2's epilogue instead of the combine kernel.
 cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide, void* out,
-                      int rows_per_expert, cudaStream_t s) {
+                      int rows_per_expert, cudaStream_t s, void* reduce_out = nullptr) {
   wide = wide && L->H % 256 == 0;
   GemmArgs a{};
   a.chunk_off = L->chunk_off;
@@ -189,6 +194,15 @@ cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
   a.pair_scale_copies = pair;
   a.stage_scales = L->stage_scales;
   a.out_rows_per_expert = rows_per_expert;
+  if (reduce_out && L->combine == MOE_COMBINE_REDUCE) {
+    a.acc = L->acc;
+    a.acc_cnt = L->acc_cnt;
+    a.prow_slot = L->prow_slot;
+    a.topk_w = L->w;
+    a.comb_out = static_cast<uint8_t*>(reduce_out);
+    a.K = L->K;
+    a.H = L->H;
+  }
   a.status = L->status;
   const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
   return launch_gemm(L->fmt, 2, L->maps2, a, grid, max_rows, wide, s);
@@ -221,6 +235,7 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
     return MOE_ERR_INVALID_ARG;
   if (c.format < MOE_FMT_BF16 || c.format > MOE_FMT_NVFP4) return MOE_ERR_INVALID_ARG;
   if (c.activation != MOE_ACT_SWIGLU && c.activation != MOE_ACT_RELU2) return MOE_ERR_INVALID_ARG;
+  if (c.combine != MOE_COMBINE_GATHER && c.combine != MOE_COMBINE_REDUCE) return MOE_ERR_INVALID_ARG;
   if (c.activation == MOE_ACT_RELU2 && c.clamp_limit > 0.0f && std::isfinite(c.clamp_limit))
     return MOE_ERR_UNSUPPORTED;
   const int kq = c.format == MOE_FMT_NVFP4 ? 256 : 128;
@@ -271,6 +286,7 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   L->NBmax = (c.max_tokens + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
   L->clamp = (c.clamp_limit > 0.0f && std::isfinite(c.clamp_limit)) ? c.clamp_limit : INFINITY;
   L->act = c.activation;
+  L->combine = c.combine;
   L->w13_rows = c.activation == MOE_ACT_RELU2 ? c.inter : 2 * c.inter;
   // MOE_PAIR_SCALE_COPIES=0 turns the decode-sized scale-copy path off.
   L->pair_scale_copies = !(pv && pv[0] == '0');
@@ -313,6 +329,10 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
             A.get(&L->h_in, static_cast<size_t>(L->Tmax) * H * 2) &&
             A.get(&L->l_in, static_cast<size_t>(L->Tmax) * E * 4) &&
             A.get(&L->o_out, static_cast<size_t>(L->Tmax) * H * 2);
+  const bool reduce = L->combine == MOE_COMBINE_REDUCE;
+  ok = ok && (!reduce || (A.get(&L->acc, static_cast<size_t>(L->Tmax) * H * 4) &&
+                          A.get(&L->acc_cnt, static_cast<size_t>(L->Tmax) * (H / 128) * 4) &&
+                          A.get(&L->prow_slot, static_cast<size_t>(Rpad) * 4)));
   if (!ok) {
     free_all(L);
     delete L;
@@ -322,7 +342,10 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   ok = cudaMemset(L->xq, 0, static_cast<size_t>(Rpad) * L->xb) == cudaSuccess &&
        cudaMemset(L->hq, 0, static_cast<size_t>(Rpad) * L->hb) == cudaSuccess &&
        cudaMemset(L->y, 0, static_cast<size_t>(Rpad) * H * 2) == cudaSuccess &&
-       cudaMemset(L->status, 0, 16) == cudaSuccess;
+       cudaMemset(L->status, 0, 16) == cudaSuccess &&
+       (!reduce || (cudaMemset(L->acc, 0, static_cast<size_t>(L->Tmax) * H * 4) == cudaSuccess &&
+                    cudaMemset(L->acc_cnt, 0, static_cast<size_t>(L->Tmax) * (H / 128) * 4) ==
+                        cudaSuccess));
   for (int i = 0; i < 4 && ok; ++i) {
     ok = make_map(&L->maps1.a[i], L->xq, L->xb, Rpad, 16u << i) &&
          make_map(&L->maps2.a[i], L->hq, L->hb, Rpad, 16u << i);
@@ -384,8 +407,8 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   if (small) {
     // one kernel for routing .. GEMM1 input (timed as the routing kernel)
     e = launch_small_front(L->fmt, logits, T, E, K, hidden, H, L->ids, L->w, L->counts,
-                           L->offsets, L->pad_off, L->chunk_off, L->perm, L->inv, L->xq, L->xsf,
-                           s);
+                           L->offsets, L->pad_off, L->chunk_off, L->perm, L->inv, L->prow_slot,
+                           L->xq, L->xsf, s);
     mark(1);
     mark(2);
   } else {
@@ -395,8 +418,8 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     mark(2);
     if (e == cudaSuccess)
       e = launch_scatter_quant(L->fmt, L->ids, T, E, K, hidden, H, L->prefix, L->counts,
-                               L->offsets, L->pad_off, L->chunk_off, L->perm, L->inv, L->xq,
-                               L->xsf, s);
+                               L->offsets, L->pad_off, L->chunk_off, L->perm, L->inv,
+                               L->prow_slot, L->xq, L->xsf, s);
     launches = 6;
   }
   mark(3);
@@ -405,9 +428,13 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && T > kPairCopyMaxTokens);
   if (e == cudaSuccess) e = run_gemm1(L, chunks, T, pair, wide, s);
   mark(4);
-  if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, wide, L->y, 0, s);
+  if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, wide, L->y, 0, s, out);
   mark(5);
-  if (e == cudaSuccess) e = launch_combine(L->y, L->inv, L->w, T, K, H, out, s);
+  // with the in-kernel reduce GEMM2 has written `out` already
+  if (e == cudaSuccess && L->combine == MOE_COMBINE_GATHER)
+    e = launch_combine(L->y, L->inv, L->w, T, K, H, out, s);
+  else
+    --launches;
   mark(6);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   L->last_T = T;

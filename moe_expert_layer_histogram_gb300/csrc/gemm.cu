@@ -302,12 +302,56 @@ __device__ __forceinline__ void epilogue_gemm2(const uint32_t* v, int p, bool st
                         pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
 }
 
+// GEMM2 with the in-kernel reduce, round p: adds w * y (fp32) of this row's
+// 64 output features into the token's fp32 accumulator (vector atomics).
+__device__ __forceinline__ void epilogue_reduce(const uint32_t* v, int p, int64_t t, float wt,
+                                                int n_tile, const GemmArgs& a) {
+  float4* dst = reinterpret_cast<float4*>(a.acc + t * a.H + n_tile * 128 + p * 64);
+#pragma unroll
+  for (int q = 0; q < 16; ++q)
+    atomicAdd(dst + q, make_float4(__fmul_rn(wt, __uint_as_float(v[4 * q])),
+                                   __fmul_rn(wt, __uint_as_float(v[4 * q + 1])),
+                                   __fmul_rn(wt, __uint_as_float(v[4 * q + 2])),
+                                   __fmul_rn(wt, __uint_as_float(v[4 * q + 3]))));
+}
+
+// After both rounds: count this contribution to the token's 128-column
+// group; the K-th contributor writes the group as bf16 and leaves the
+// accumulator and its counter at zero for the next forward.
+__device__ __forceinline__ void reduce_finish(int64_t t, int n_tile, const GemmArgs& a) {
+  __threadfence();
+  int32_t* cnt = a.acc_cnt + t * (a.H / 128) + n_tile;
+  if (atomicAdd(cnt, 1) != a.K - 1) return;
+  __threadfence();
+  float4* acc = reinterpret_cast<float4*>(a.acc + t * a.H + n_tile * 128);
+  uint4* out = reinterpret_cast<uint4*>(a.comb_out + (t * a.H + n_tile * 128) * 2);
+#pragma unroll 4
+  for (int q = 0; q < 16; ++q) {
+    const float4 x = __ldcg(acc + 2 * q), y = __ldcg(acc + 2 * q + 1);
+    out[q] = make_uint4(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w), pack_bf16x2(y.x, y.y),
+                        pack_bf16x2(y.z, y.w));
+    __stcg(acc + 2 * q, make_float4(0.f, 0.f, 0.f, 0.f));
+    __stcg(acc + 2 * q + 1, make_float4(0.f, 0.f, 0.f, 0.f));
+  }
+  *cnt = 0;
+}
+
 template <int FMT, int EPI>
 __device__ __forceinline__ void epilogue_round(const uint32_t* v, int p, bool store, int64_t prow,
                                                int64_t orow, int n_tile, const GemmArgs& a) {
-  if constexpr (EPI == 1) epilogue_gemm1<FMT>(v, p, store, prow, n_tile, a);
-  else if constexpr (EPI == 3) epilogue_relu2<FMT>(v, p, store, prow, n_tile, a);
-  else epilogue_gemm2(v, p, store, orow, n_tile, a);
+  if constexpr (EPI == 1) {
+    epilogue_gemm1<FMT>(v, p, store, prow, n_tile, a);
+  } else if constexpr (EPI == 3) {
+    epilogue_relu2<FMT>(v, p, store, prow, n_tile, a);
+  } else if (a.acc) {
+    if (store) {
+      const int slot = a.prow_slot[prow];
+      epilogue_reduce(v, p, slot / a.K, a.topk_w[slot], n_tile, a);
+      if (p == 1) reduce_finish(slot / a.K, n_tile, a);
+    }
+  } else {
+    epilogue_gemm2(v, p, store, orow, n_tile, a);
+  }
 }
 
 // ---------------------------------------------------------------- kernel

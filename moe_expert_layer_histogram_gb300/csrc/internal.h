@@ -48,6 +48,15 @@ struct GemmArgs {
   float clamp;               // +inf: no clamp
   int pair_scale_copies;     // 1: chunks of <= 32 rows need scales in lanes 0-31 only
   int stage_scales;          // 1: ... which a dedicated warp writes there (tcgen05.st)
+  // GEMM2 with the in-kernel reduce (acc != nullptr): out[t] = bf16(sum_k
+  // w[t,k] * y), summed in `acc` (fp32 [T, H], zero between forwards) with
+  // atomics; acc_cnt [T, H/128] counts contributions per 128-column group.
+  float* acc;
+  int32_t* acc_cnt;
+  const int32_t* prow_slot;  // padded row -> slot t*K + k
+  const float* topk_w;       // [T*K]
+  uint8_t* comb_out;         // bf16 [T, H]
+  int K, H;
   int test_stall;            // test hook: CTA 0 never loads one stage, so the waits on it
                              // run out (bounded) and the kernel reports a timeout
   int out_rows_per_expert;   // 0: output row = padded row; M > 0 (batched format):
@@ -116,19 +125,20 @@ cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids,
                          int32_t* blockhist, cudaStream_t s);
 cudaError_t launch_expert_scan(const int32_t* blockhist, int NB, int E, int32_t* prefix,
                                int32_t* counts, cudaStream_t s);
+// prow_slot (may be null): padded row -> slot, for the in-kernel reduce.
 cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int K,
                                  const void* hidden, int H, const int32_t* prefix,
                                  const int32_t* counts, int32_t* offsets, int32_t* pad_off,
-                                 int32_t* chunk_off, int32_t* perm, int32_t* inv, uint8_t* xq,
-                                 uint8_t* xsf, cudaStream_t s);
+                                 int32_t* chunk_off, int32_t* perm, int32_t* inv,
+                                 int32_t* prow_slot, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int K, int H,
                            void* out, cudaStream_t s);
 // T <= kSmallFrontTokens: routing, scans, ranks and GEMM1 input in one block.
 cudaError_t launch_small_front(int fmt, const float* logits, int T, int E, int K,
                                const void* hidden, int H, int32_t* ids, float* w,
                                int32_t* counts, int32_t* offsets, int32_t* pad_off,
-                               int32_t* chunk_off, int32_t* perm, int32_t* inv, uint8_t* xq,
-                               uint8_t* xsf, cudaStream_t s);
+                               int32_t* chunk_off, int32_t* perm, int32_t* inv,
+                               int32_t* prow_slot, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
 // Batched-expert format: per-expert tables from the counts and the GEMM1
 // input rows of hidden [E, M, H].
 cudaError_t launch_batched_quant(int fmt, const void* hidden, const int32_t* counts_in, int M,

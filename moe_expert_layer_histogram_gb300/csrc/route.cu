@@ -251,8 +251,8 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
     const int32_t* __restrict__ ids, int T, int E, int K, const __nv_bfloat16* __restrict__ hidden,
     int H, const int32_t* __restrict__ prefix, const int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ pad_off, int32_t* __restrict__ chunk_off,
-    int32_t* __restrict__ perm, int32_t* __restrict__ inv, uint8_t* __restrict__ xq,
-    uint8_t* __restrict__ xsf) {
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ prow_slot,
+    uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts], cnt[kMaxExperts];
@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
         perm[s_off[e] + r] = static_cast<int32_t>(s);
         const int prow = s_poff[e] + r;
         inv[s] = prow;
+        if (prow_slot) prow_slot[prow] = static_cast<int32_t>(s);
         s_prow[i * K + lane] = prow;
       }
       __syncwarp();
@@ -335,8 +336,8 @@ __global__ void __launch_bounds__(256) small_front_kernel(
     const float* __restrict__ logits, int T, int E, int K, const __nv_bfloat16* __restrict__ hidden,
     int H, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ pad_off, int32_t* __restrict__ chunk_off,
-    int32_t* __restrict__ perm, int32_t* __restrict__ inv, uint8_t* __restrict__ xq,
-    uint8_t* __restrict__ xsf) {
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ prow_slot,
+    uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
   pdl_launch_dependents();
   __shared__ int hist[kMaxExperts], cnt[kMaxExperts], s_off[kMaxExperts], s_poff[kMaxExperts];
   __shared__ int s_ids[kSmallFrontTokens * kMaxTopK], s_prow[kSmallFrontTokens * kMaxTopK];
@@ -412,6 +413,7 @@ __global__ void __launch_bounds__(256) small_front_kernel(
         if (store) {
           perm[s_off[e] + r] = s;
           inv[s] = prow;
+          if (prow_slot) prow_slot[prow] = s;
         }
         s_prow[s] = prow;
       }
@@ -605,22 +607,22 @@ cudaError_t launch_expert_scan(const int32_t* blockhist, int NB, int E, int32_t*
 cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int K,
                                  const void* hidden, int H, const int32_t* prefix,
                                  const int32_t* counts, int32_t* offsets, int32_t* pad_off,
-                                 int32_t* chunk_off, int32_t* perm, int32_t* inv, uint8_t* xq,
-                                 uint8_t* xsf, cudaStream_t s) {
+                                 int32_t* chunk_off, int32_t* perm, int32_t* inv,
+                                 int32_t* prow_slot, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
   const int nb = (T + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
   const auto* hb = static_cast<const __nv_bfloat16*>(hidden);
   auto k = fmt == kFmtBF16 ? scatter_quant_kernel<kFmtBF16>
            : fmt == kFmtMXFP8 ? scatter_quant_kernel<kFmtMXFP8>
                               : scatter_quant_kernel<kFmtNVFP4>;
   return launch_pdl(g_pdl_small, k, dim3(nb), dim3(256), 0, s, ids, T, E, K, hb, H, prefix,
-                    counts, offsets, pad_off, chunk_off, perm, inv, xq, xsf);
+                    counts, offsets, pad_off, chunk_off, perm, inv, prow_slot, xq, xsf);
 }
 
 cudaError_t launch_small_front(int fmt, const float* logits, int T, int E, int K,
                                const void* hidden, int H, int32_t* ids, float* w,
                                int32_t* counts, int32_t* offsets, int32_t* pad_off,
-                               int32_t* chunk_off, int32_t* perm, int32_t* inv, uint8_t* xq,
-                               uint8_t* xsf, cudaStream_t s) {
+                               int32_t* chunk_off, int32_t* perm, int32_t* inv,
+                               int32_t* prow_slot, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
   if (T > kSmallFrontTokens) return cudaErrorInvalidValue;
   const auto* hb = static_cast<const __nv_bfloat16*>(hidden);
   auto pick = [&](auto k4, auto k8, auto k16) { return E <= 128 ? k4 : E <= 256 ? k8 : k16; };
@@ -633,7 +635,7 @@ cudaError_t launch_small_front(int fmt, const float* logits, int T, int E, int K
                : pick(small_front_kernel<kFmtNVFP4, 4>, small_front_kernel<kFmtNVFP4, 8>,
                       small_front_kernel<kFmtNVFP4, 16>);
   return launch_pdl(g_pdl_small, k, dim3(T), dim3(256), 0, s, logits, T, E, K, hb, H, ids, w,
-                    counts, offsets, pad_off, chunk_off, perm, inv, xq, xsf);
+                    counts, offsets, pad_off, chunk_off, perm, inv, prow_slot, xq, xsf);
 }
 
 cudaError_t launch_batched_quant(int fmt, const void* hidden, const int32_t* counts_in, int M,

@@ -28,7 +28,7 @@ def make_layer(s, max_tokens=None, weights=None, device="cuda:0"):
     import torch
     from moe_expert_layer_histogram_gb300 import MoELayer
     layer = MoELayer(max_tokens or s["T"], s["H"], s["I"], s["E"], s["K"], s["fmt"], s["clamp"],
-                     s.get("act", "swiglu"))
+                     s.get("act", "swiglu"), s.get("combine", "gather"))
     if weights is not None:
         layer.prepare_weights({k: v.to(device).contiguous() for k, v in weights.items()})
     torch.cuda.synchronize()

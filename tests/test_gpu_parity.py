@@ -377,3 +377,30 @@ def test_wide_items_batched_format(monkeypatch):
         mask[e, :cn[e]] = True
     assert rel_l2(got[mask], ref["y"][mask]) <= TOL["nvfp4"]
     layer.close()
+
+
+# ---- the in-kernel reduce (GEMM2's epilogue sums the K outputs) ------------
+@pytest.mark.parametrize("name,over,wide", [
+    ("bf16_small", dict(combine="reduce"), False),
+    ("mxfp8_small", dict(combine="reduce"), False),
+    ("nvfp4_small", dict(combine="reduce"), False),
+    ("nvfp4_small", dict(T=7, E=300, K=8, combine="reduce"), False),    # one-kernel front end
+    ("nvfp4_small", dict(combine="reduce", act="relu2"), True),
+    ("bf16_small", dict(T=300, E=4, K=2, combine="reduce"), True),
+], ids=["bf16", "mxfp8", "nvfp4", "nvfp4-T7", "nvfp4-relu2-wide", "bf16-chunks-wide"])
+def test_in_kernel_reduce_matches_oracle(name, over, wide, monkeypatch):
+    if wide:
+        monkeypatch.setenv("MOE_WIDE_TILES", "1")
+    s = workloads.spec(name, **over)
+    case = workloads.make_case(s, seed=17)
+    ref = run_oracle(s, case)
+    layer = make_layer(s, weights=case["weights"])
+    outs = []
+    for _ in range(3):                   # the accumulator is left at zero between forwards
+        outs.append(run_gpu(layer, case["hidden"], case["logits"]).float().cpu().numpy())
+    assert layer.status() == 0
+    for o in outs:
+        assert rel_l2(o, bf16_bits_to_f64(ref["out"])) <= TOL[s["fmt"]]
+    # only the summation order differs between runs: last-bit differences at most
+    assert max(np.max(np.abs(o - outs[0])) for o in outs) <= 1e-2 * np.max(np.abs(outs[0]))
+    layer.close()
