@@ -43,6 +43,8 @@ struct moe_layer {
   int combine = MOE_COMBINE_GATHER;
   float* acc = nullptr;              // in-kernel reduce: fp32 [Tmax, H], zero between forwards
   int32_t *acc_cnt = nullptr, *prow_slot = nullptr;
+  int32_t* done1 = nullptr;          // fused decode GEMMs: per-expert GEMM1 completion counts
+  int fused_gemms = 1;               // T <= 16: GEMM1 and GEMM2 in one launch
   float* w = nullptr;
   uint8_t *xq = nullptr, *xsf = nullptr, *hq = nullptr, *hsf = nullptr, *y = nullptr;
   uint8_t *w13t = nullptr, *w2t = nullptr;  // prepared weight tiles
@@ -137,11 +139,8 @@ int64_t max_chunks(const moe_layer* L, int T) {
 }
 
 // GEMM1 (+ the activation and re-quantisation) over the padded
-// activation rows of the current tables.  max_rows bounds the rows of any
-// expert (selects the activation tile height).
-cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide,
-                      cudaStream_t s) {
-  wide = wide && L->w13_rows % 256 == 0;
+// activation rows of the current tables.
+GemmArgs gemm1_args(const moe_layer* L, int pair, bool wide) {
   GemmArgs a{};
   a.chunk_off = L->chunk_off;
   a.pad_off = L->pad_off;
@@ -163,18 +162,15 @@ cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
   a.test_stall = L->test_stall;
   a.out_rows_per_expert = 0;
   a.status = L->status;
-  const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
-  return launch_gemm(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a, grid, max_rows, wide,
-                     s);
+  return a;
 }
 
 // GEMM2 into `out` (bf16, H per row): padded rows (rows_per_expert 0) or
-// rows e*rows_per_expert + i (batched format).
-// reduce_out (routed forward with the in-kernel reduce): the bf16 layer
-// output, summed by GEMM2's epilogue instead of the combine kernel.
-cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide, void* out,
-                      int rows_per_expert, cudaStream_t s, void* reduce_out = nullptr) {
-  wide = wide && L->H % 256 == 0;
+// rows e*rows_per_expert + i (batched format).  reduce_out (routed forward
+// with the in-kernel reduce): the bf16 layer output, summed by GEMM2's
+// epilogue instead of the combine kernel.
+GemmArgs gemm2_args(const moe_layer* L, int pair, bool wide, void* out, int rows_per_expert,
+                    void* reduce_out) {
   GemmArgs a{};
   a.chunk_off = L->chunk_off;
   a.pad_off = L->pad_off;
@@ -204,8 +200,38 @@ cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
     a.H = L->H;
   }
   a.status = L->status;
+  return a;
+}
+
+// max_rows bounds the rows of any expert (selects the activation tile height).
+cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide,
+                      cudaStream_t s) {
+  wide = wide && L->w13_rows % 256 == 0;
+  const GemmArgs a = gemm1_args(L, pair, wide);
+  const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
+  return launch_gemm(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a, grid, max_rows, wide,
+                     s);
+}
+
+cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide, void* out,
+                      int rows_per_expert, cudaStream_t s, void* reduce_out = nullptr) {
+  wide = wide && L->H % 256 == 0;
+  const GemmArgs a = gemm2_args(L, pair, wide, out, rows_per_expert, reduce_out);
   const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
   return launch_gemm(L->fmt, 2, L->maps2, a, grid, max_rows, wide, s);
+}
+
+// Decode: GEMM1 and GEMM2 in one persistent launch (narrow items, chunks of
+// at most 32 rows); the front end has zeroed the per-expert counters.
+cudaError_t run_gemms_fused(moe_layer* L, int64_t chunks, int pair, void* reduce_out,
+                            cudaStream_t s) {
+  GemmArgs a1 = gemm1_args(L, pair, false);
+  a1.done1 = L->done1;
+  const GemmArgs a2 = gemm2_args(L, pair, false, L->y, 0, reduce_out);
+  const int grid = static_cast<int>(
+      std::min<int64_t>(L->num_sms, chunks * (a1.n_tiles + a2.n_tiles)));
+  return launch_gemm_fused(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a1, L->maps2, a2,
+                           grid, s);
 }
 
 }  // namespace
@@ -300,6 +326,8 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   // every GEMM1 launch leave one stage unloaded; its waits give up after
   // 2 s and moe_get_status reports MOE_ERR_DEVICE_TIMEOUT.
   if (const char* tv = std::getenv("MOE_TEST_STALL_GEMM")) L->test_stall = tv[0] == '1';
+  // MOE_FUSED_GEMMS=0: decode launches keep GEMM1 and GEMM2 separate.
+  if (const char* fv = std::getenv("MOE_FUSED_GEMMS")) L->fused_gemms = fv[0] != '0';
   const int H = L->H, I = L->I, E = L->E;
   if (L->fmt == MOE_FMT_NVFP4) {
     L->xb = H / 2; L->hb = I / 2; L->x_tiles_k = H / 64; L->h_tiles_k = I / 64;
@@ -328,7 +356,8 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
             A.get(&L->status, 16) &&
             A.get(&L->h_in, static_cast<size_t>(L->Tmax) * H * 2) &&
             A.get(&L->l_in, static_cast<size_t>(L->Tmax) * E * 4) &&
-            A.get(&L->o_out, static_cast<size_t>(L->Tmax) * H * 2);
+            A.get(&L->o_out, static_cast<size_t>(L->Tmax) * H * 2) &&
+            A.get(&L->done1, static_cast<size_t>(E) * 4);
   const bool reduce = L->combine == MOE_COMBINE_REDUCE;
   ok = ok && (!reduce || (A.get(&L->acc, static_cast<size_t>(L->Tmax) * H * 4) &&
                           A.get(&L->acc_cnt, static_cast<size_t>(L->Tmax) * (H / 128) * 4) &&
@@ -408,7 +437,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     // one kernel for routing .. GEMM1 input (timed as the routing kernel)
     e = launch_small_front(L->fmt, logits, T, E, K, hidden, H, L->ids, L->w, L->counts,
                            L->offsets, L->pad_off, L->chunk_off, L->perm, L->inv, L->prow_slot,
-                           L->xq, L->xsf, s);
+                           L->done1, L->xq, L->xsf, s);
     mark(1);
     mark(2);
   } else {
@@ -426,9 +455,17 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   const int64_t chunks = max_chunks(L, T);
   const int pair = L->pair_scale_copies && T <= kPairCopyMaxTokens;
   const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && T > kPairCopyMaxTokens);
-  if (e == cudaSuccess) e = run_gemm1(L, chunks, T, pair, wide, s);
-  mark(4);
-  if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, wide, L->y, 0, s, out);
+  void* reduce_out = L->combine == MOE_COMBINE_REDUCE ? out : nullptr;
+  if (small && !wide && L->fused_gemms) {
+    // one launch for both GEMMs (timed as GEMM1)
+    if (e == cudaSuccess) e = run_gemms_fused(L, chunks, pair, reduce_out, s);
+    --launches;
+    mark(4);
+  } else {
+    if (e == cudaSuccess) e = run_gemm1(L, chunks, T, pair, wide, s);
+    mark(4);
+    if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, wide, L->y, 0, s, out);
+  }
   mark(5);
   // with the in-kernel reduce GEMM2 has written `out` already
   if (e == cudaSuccess && L->combine == MOE_COMBINE_GATHER)

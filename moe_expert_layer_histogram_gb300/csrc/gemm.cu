@@ -355,9 +355,17 @@ __device__ __forceinline__ void epilogue_round(const uint32_t* v, int p, bool st
 }
 
 // ---------------------------------------------------------------- kernel
-template <int FMT, int EPI, int MROWS, int NW>
+// FUSED (decode): one launch runs GEMM1's items (args/maps) and then
+// GEMM2's (args2/maps2).  Each CTA finishes issuing its GEMM1 items before
+// its GEMM2 items; a GEMM2 item of expert e waits (bounded) until every
+// GEMM1 item of expert e has stored its output, counted in args.done1[e] by
+// each epilogue warp.  CTAs whose GEMM1 share ends early move on to GEMM2
+// work instead of idling until the slowest CTA finishes.
+template <int FMT, int EPI, int MROWS, int NW, bool FUSED>
 __global__ void __launch_bounds__(gemm_threads(NW), 1)
-    moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
+    moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs args,
+                    const __grid_constant__ GemmMaps maps2,
+                    const __grid_constant__ GemmArgs args2) {
   constexpr int SFT = Fmt<FMT>::kSfTiles;
   constexpr int SB = stage_bytes<FMT, MROWS, NW>();
   constexpr int kStages = num_stages<FMT, MROWS, NW>();
@@ -414,7 +422,12 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const int total = tab.chunk_off[args.E] * args.n_tiles;
+  const int n1 = tab.chunk_off[args.E] * args.n_tiles;  // GEMM1 (or the only GEMM) items
+  const int total = FUSED ? n1 + tab.chunk_off[args.E] * args2.n_tiles : n1;
+  // item -> (GEMM, item within it)
+  auto second = [&](int item) { return FUSED && item >= n1; };
+  auto local_item = [&](int item) { return second(item) ? item - n1 : item; };
+  auto gargs = [&](int item) -> const GemmArgs& { return second(item) ? args2 : args; };
   // Decode launches: a chunk of at most 32 rows keeps all its real
   // accumulator rows in TMEM lane quarter 0, and the MMA of each lane quarter
   // reads both operands' scales from that quarter's own lanes, so such a
@@ -432,8 +445,9 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const bool q0 = map_item(tab, args.E, args.n_tiles, item).rows <= 32;
-        for (int kb = 0; kb < args.num_kb; ++kb) {
+        const GemmArgs& A = gargs(item);
+        const bool q0 = map_item(tab, args.E, A.n_tiles, local_item(item)).rows <= 32;
+        for (int kb = 0; kb < A.num_kb; ++kb) {
           const bool landed = mbar_wait(&full[stage], phase, abort_flag);
           if (!__all_sync(0xFFFFFFFFu, landed)) {
             ok = false;
@@ -492,25 +506,36 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
       int skipped = -1;       // position the test hook left unloaded
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const Item it = map_item(tab, args.E, args.n_tiles, item);
+        const GemmArgs& A = gargs(item);
+        const CUtensorMap* amaps = second(item) ? maps2.a : maps.a;
+        const Item it = map_item(tab, args.E, A.n_tiles, local_item(item));
         const int amap = it.rows <= 16 ? 0 : it.rows <= 32 ? 1 : it.rows <= 64 ? 2 : 3;
         if ((16 << amap) > MROWS) {   // the host bounded the rows per chunk by MROWS
           ok = false;
           break;
         }
-        const uint32_t bytes = (16u << amap) * 128u + NW * args.b_tile_bytes + SFT * 512u;
-        const uint8_t* sfa = args.sfa + static_cast<int64_t>(it.prow0 >> 7) * args.sfa_tiles_k * 512;
+        if (second(item)) {
+          // GEMM2's activations are GEMM1's output for this expert
+          const int need = 4 * args.n_tiles * (tab.chunk_off[it.e + 1] - tab.chunk_off[it.e]);
+          if (!wait_count_at_least(args.done1 + it.e, need, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();  // generic-proxy stores -> the TMA reads below
+        }
+        const uint32_t bytes = (16u << amap) * 128u + NW * A.b_tile_bytes + SFT * 512u;
+        const uint8_t* sfa = A.sfa + static_cast<int64_t>(it.prow0 >> 7) * A.sfa_tiles_k * 512;
         // the item's first 128-row weight tile; the next one (NW = 2)
         // follows num_kb tiles later
         const uint8_t* btile =
-            args.b_tiles + (static_cast<int64_t>(it.e) * args.n_tiles + it.n_tile) * NW *
-                               args.num_kb * args.b_tile_bytes;
-        for (int kb = 0; kb < args.num_kb; ++kb) {
+            A.b_tiles + (static_cast<int64_t>(it.e) * A.n_tiles + it.n_tile) * NW * A.num_kb *
+                            A.b_tile_bytes;
+        for (int kb = 0; kb < A.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          if (args.test_stall && blockIdx.x == 0 && skipped < 0) {
+          if (A.test_stall && blockIdx.x == 0 && skipped < 0) {
             // test hook: nothing ever completes this stage
             skipped = slots++;
             if (++stage == kStages) {
@@ -521,18 +546,18 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
           }
           uint8_t* sp = smem + stage * SB;
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(sp, &maps.a[amap], &full[stage], kb * 128, it.prow0);
+          tma_load_2d(sp, &amaps[amap], &full[stage], kb * 128, it.prow0);
           if constexpr (NW == 1) {
             // weight tile codes + its scale tiles: one contiguous block
-            bulk_load_hint(sp + A_BYTES, btile + static_cast<int64_t>(kb) * args.b_tile_bytes,
-                           args.b_tile_bytes, &full[stage], policy);
+            bulk_load_hint(sp + A_BYTES, btile + static_cast<int64_t>(kb) * A.b_tile_bytes,
+                           A.b_tile_bytes, &full[stage], policy);
           } else {
             // codes of both tiles back to back (one 256-row operand), then
             // their scale tiles
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
               const uint8_t* src =
-                  btile + (static_cast<int64_t>(w) * args.num_kb + kb) * args.b_tile_bytes;
+                  btile + (static_cast<int64_t>(w) * A.num_kb + kb) * A.b_tile_bytes;
               bulk_load_hint(sp + A_BYTES + w * kTileBytes, src, kTileBytes, &full[stage], policy);
               if constexpr (SFT > 0)
                 bulk_load_hint(sp + kOffBsf + w * SFT * 512, src + kTileBytes, SFT * 512,
@@ -569,6 +594,7 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
       int local = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++local) {
+        const GemmArgs& A = gargs(item);
         const int buf = local % kBufs;
         const uint32_t use = static_cast<uint32_t>(local / kBufs);
         // A chunk of at most 32 rows keeps all its real accumulator rows in
@@ -579,14 +605,14 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
         // shared memory and only feed accumulator rows that are not stored).
         // Larger chunks broadcast every tile to all four quarters.
         const bool q0_only = NW == 1 && args.pair_scale_copies &&
-                             map_item(tab, args.E, args.n_tiles, item).rows <= 32;
+                             map_item(tab, args.E, A.n_tiles, local_item(item)).rows <= 32;
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * kAccCols;
-        for (int kb = 0; kb < args.num_kb; ++kb) {
+        for (int kb = 0; kb < A.num_kb; ++kb) {
           if (!mbar_wait(staged ? &sf_ready[stage] : &full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -687,7 +713,9 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
     const int grp = (warp - 3) >> 2;
     int local = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++local) {
-      const Item it = map_item(tab, args.E, args.n_tiles, item);
+      const GemmArgs& A = gargs(item);
+      const bool g2 = second(item);
+      const Item it = map_item(tab, args.E, A.n_tiles, local_item(item));
       const int buf = local % kBufs;
       const uint32_t use = static_cast<uint32_t>(local / kBufs);
       if (!mbar_wait(&tfull[buf], use & 1u, abort_flag)) {
@@ -701,8 +729,8 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
           tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols + grp * 128;
       const int64_t prow = it.prow0 + r;
       // batched format: expert e's rows go to rows e*M.. of the output
-      const int64_t orow = args.out_rows_per_expert
-                               ? static_cast<int64_t>(it.e) * args.out_rows_per_expert +
+      const int64_t orow = A.out_rows_per_expert
+                               ? static_cast<int64_t>(it.e) * A.out_rows_per_expert +
                                      (it.prow0 - tab.pad_off[it.e]) + r
                                : prow;
       const int n128 = it.n_tile * NW + grp;
@@ -711,15 +739,23 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             uint32_t v[64];
-            epilogue_load<EPI>(taddr, p, v);
+            if (g2) epilogue_load<2>(taddr, p, v);
+            else epilogue_load<EPI>(taddr, p, v);
             tmem_ld_wait();
             epilogue_fence(v);
-            epilogue_round<FMT, EPI>(v, p, r < it.rows, prow, orow, n128, args);
+            if (g2) epilogue_round<FMT, 2>(v, p, r < it.rows, prow, orow, n128, A);
+            else epilogue_round<FMT, EPI>(v, p, r < it.rows, prow, orow, n128, A);
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (FUSED && !g2) {
+          // this warp's rows of the item are stored: count them for GEMM2
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) atomicAdd(args.done1 + it.e, 1);
+        }
       } else {
         uint32_t v[128];
         if (active) {
@@ -734,8 +770,8 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
         if (active) {
-          epilogue_round<FMT, EPI>(v, 0, r < it.rows, prow, orow, n128, args);
-          epilogue_round<FMT, EPI>(v + 64, 1, r < it.rows, prow, orow, n128, args);
+          epilogue_round<FMT, EPI>(v, 0, r < it.rows, prow, orow, n128, A);
+          epilogue_round<FMT, EPI>(v + 64, 1, r < it.rows, prow, orow, n128, A);
         }
       }
     }
@@ -747,15 +783,17 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int FMT, int EPI, int MROWS, int NW>
-cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t s) {
-  return launch_pdl(g_pdl_gemm, moe_gemm_kernel<FMT, EPI, MROWS, NW>, dim3(grid),
-                    dim3(gemm_threads(NW)), smem_bytes<FMT, MROWS, NW>(), s, maps, args);
+template <int FMT, int EPI, int MROWS, int NW, bool FUSED = false>
+cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, const GemmMaps& maps2,
+                       const GemmArgs& args2, int grid, cudaStream_t s) {
+  return launch_pdl(g_pdl_gemm, moe_gemm_kernel<FMT, EPI, MROWS, NW, FUSED>, dim3(grid),
+                    dim3(gemm_threads(NW)), smem_bytes<FMT, MROWS, NW>(), s, maps, args, maps2,
+                    args2);
 }
 
-template <int FMT, int EPI, int MROWS, int NW>
+template <int FMT, int EPI, int MROWS, int NW, bool FUSED = false>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(moe_gemm_kernel<FMT, EPI, MROWS, NW>,
+  return cudaFuncSetAttribute(moe_gemm_kernel<FMT, EPI, MROWS, NW, FUSED>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               smem_bytes<FMT, MROWS, NW>());
 }
@@ -774,16 +812,18 @@ cudaError_t prepare_one() {
   if (e == cudaSuccess) e = prepare_m<FMT, 64, 1>();
   if (e == cudaSuccess) e = prepare_m<FMT, 128, 1>();
   if (e == cudaSuccess) e = prepare_m<FMT, 128, 2>();
+  if (e == cudaSuccess) e = set_smem<FMT, 1, 32, 1, true>();
+  if (e == cudaSuccess) e = set_smem<FMT, 3, 32, 1, true>();
   return e;
 }
 
 template <int FMT, int EPI>
 cudaError_t launch_fmt(const GemmMaps& maps, const GemmArgs& args, int grid, int mrows, bool wide,
                        cudaStream_t s) {
-  if (wide) return launch_one<FMT, EPI, 128, 2>(maps, args, grid, s);
-  if (mrows <= 32) return launch_one<FMT, EPI, 32, 1>(maps, args, grid, s);
-  if (mrows <= 64) return launch_one<FMT, EPI, 64, 1>(maps, args, grid, s);
-  return launch_one<FMT, EPI, 128, 1>(maps, args, grid, s);
+  if (wide) return launch_one<FMT, EPI, 128, 2>(maps, args, maps, args, grid, s);
+  if (mrows <= 32) return launch_one<FMT, EPI, 32, 1>(maps, args, maps, args, grid, s);
+  if (mrows <= 64) return launch_one<FMT, EPI, 64, 1>(maps, args, maps, args, grid, s);
+  return launch_one<FMT, EPI, 128, 1>(maps, args, maps, args, grid, s);
 }
 
 template <int FMT>
@@ -807,6 +847,19 @@ cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& 
   if (fmt == kFmtBF16) return launch_epi<kFmtBF16>(epi, maps, args, grid, max_rows, wide, s);
   if (fmt == kFmtMXFP8) return launch_epi<kFmtMXFP8>(epi, maps, args, grid, max_rows, wide, s);
   return launch_epi<kFmtNVFP4>(epi, maps, args, grid, max_rows, wide, s);
+}
+
+cudaError_t launch_gemm_fused(int fmt, int epi1, const GemmMaps& maps1, const GemmArgs& args1,
+                              const GemmMaps& maps2, const GemmArgs& args2, int grid,
+                              cudaStream_t s) {
+  if (fmt == kFmtBF16)
+    return epi1 == 3 ? launch_one<kFmtBF16, 3, 32, 1, true>(maps1, args1, maps2, args2, grid, s)
+                     : launch_one<kFmtBF16, 1, 32, 1, true>(maps1, args1, maps2, args2, grid, s);
+  if (fmt == kFmtMXFP8)
+    return epi1 == 3 ? launch_one<kFmtMXFP8, 3, 32, 1, true>(maps1, args1, maps2, args2, grid, s)
+                     : launch_one<kFmtMXFP8, 1, 32, 1, true>(maps1, args1, maps2, args2, grid, s);
+  return epi1 == 3 ? launch_one<kFmtNVFP4, 3, 32, 1, true>(maps1, args1, maps2, args2, grid, s)
+                   : launch_one<kFmtNVFP4, 1, 32, 1, true>(maps1, args1, maps2, args2, grid, s);
 }
 
 }  // namespace moe

@@ -57,6 +57,7 @@ struct GemmArgs {
   const float* topk_w;       // [T*K]
   uint8_t* comb_out;         // bf16 [T, H]
   int K, H;
+  int32_t* done1;            // fused GEMM1+GEMM2 launch: per expert, GEMM1 epilogue warps done
   int test_stall;            // test hook: CTA 0 never loads one stage, so the waits on it
                              // run out (bounded) and the kernel reports a timeout
   int out_rows_per_expert;   // 0: output row = padded row; M > 0 (batched format):
@@ -119,6 +120,11 @@ cudaError_t gemm_prepare(int fmt);  // raise the dynamic shared-memory limit
 // whose chunks are mostly full 128-row blocks.
 cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& args, int grid,
                         int max_rows, bool wide, cudaStream_t s);
+// Decode (chunks of <= 32 rows, narrow items): GEMM1 (epi1 = 1 or 3) and
+// GEMM2 in one persistent launch; args1.done1 must be zero per expert.
+cudaError_t launch_gemm_fused(int fmt, int epi1, const GemmMaps& maps1, const GemmArgs& args1,
+                              const GemmMaps& maps2, const GemmArgs& args2, int grid,
+                              cudaStream_t s);
 
 // Routing, permutation + activation quantisation, combine.
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* w,
@@ -134,11 +140,14 @@ cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int 
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int K, int H,
                            void* out, cudaStream_t s);
 // T <= kSmallFrontTokens: routing, scans, ranks and GEMM1 input in one block.
+// done1 (may be null): per-expert counters of a following fused GEMM launch,
+// zeroed here.
 cudaError_t launch_small_front(int fmt, const float* logits, int T, int E, int K,
                                const void* hidden, int H, int32_t* ids, float* w,
                                int32_t* counts, int32_t* offsets, int32_t* pad_off,
                                int32_t* chunk_off, int32_t* perm, int32_t* inv,
-                               int32_t* prow_slot, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+                               int32_t* prow_slot, int32_t* done1, uint8_t* xq, uint8_t* xsf,
+                               cudaStream_t s);
 // Batched-expert format: per-expert tables from the counts and the GEMM1
 // input rows of hidden [E, M, H].
 cudaError_t launch_batched_quant(int fmt, const void* hidden, const int32_t* counts_in, int M,

@@ -74,6 +74,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Wait until *counter >= need (a count other CTAs of the grid raise after
+// storing their results).  Bounded like mbar_wait: false after
+// kWaitTimeoutNs (sets *abort) or when another role gave up.
+__device__ __forceinline__ bool wait_count_at_least(const int* counter, int need,
+                                                    volatile int* abort) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    if (v >= need) return true;
+    if ((i & 63u) == 63u) {
+      if (abort && *abort) return false;
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if (abort) *abort = 1;
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
+
+// Order this thread's earlier generic-proxy view of global memory before
+// its later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t x, int32_t y) {

@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(256) small_front_kernel(
     int H, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ pad_off, int32_t* __restrict__ chunk_off,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ prow_slot,
-    uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
+    int32_t* __restrict__ done1, uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
   pdl_launch_dependents();
   __shared__ int hist[kMaxExperts], cnt[kMaxExperts], s_off[kMaxExperts], s_poff[kMaxExperts];
   __shared__ int s_ids[kSmallFrontTokens * kMaxTopK], s_prow[kSmallFrontTokens * kMaxTopK];
@@ -381,6 +381,10 @@ __global__ void __launch_bounds__(256) small_front_kernel(
     s_poff[e1] = xp + p0 * kRowBlock;
   }
   if (store) {
+    if (done1) {
+      if (e0 < E) done1[e0] = 0;
+      if (e1 < E) done1[e1] = 0;
+    }
     if (e0 < E) {
       counts[e0] = c0;
       offsets[e0] = xo;
@@ -622,7 +626,8 @@ cudaError_t launch_small_front(int fmt, const float* logits, int T, int E, int K
                                const void* hidden, int H, int32_t* ids, float* w,
                                int32_t* counts, int32_t* offsets, int32_t* pad_off,
                                int32_t* chunk_off, int32_t* perm, int32_t* inv,
-                               int32_t* prow_slot, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+                               int32_t* prow_slot, int32_t* done1, uint8_t* xq, uint8_t* xsf,
+                               cudaStream_t s) {
   if (T > kSmallFrontTokens) return cudaErrorInvalidValue;
   const auto* hb = static_cast<const __nv_bfloat16*>(hidden);
   auto pick = [&](auto k4, auto k8, auto k16) { return E <= 128 ? k4 : E <= 256 ? k8 : k16; };
@@ -635,7 +640,7 @@ cudaError_t launch_small_front(int fmt, const float* logits, int T, int E, int K
                : pick(small_front_kernel<kFmtNVFP4, 4>, small_front_kernel<kFmtNVFP4, 8>,
                       small_front_kernel<kFmtNVFP4, 16>);
   return launch_pdl(g_pdl_small, k, dim3(T), dim3(256), 0, s, logits, T, E, K, hb, H, ids, w,
-                    counts, offsets, pad_off, chunk_off, perm, inv, prow_slot, xq, xsf);
+                    counts, offsets, pad_off, chunk_off, perm, inv, prow_slot, done1, xq, xsf);
 }
 
 cudaError_t launch_batched_quant(int fmt, const void* hidden, const int32_t* counts_in, int M,
