@@ -222,16 +222,17 @@ cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
 }
 
 // Decode: GEMM1 and GEMM2 in one persistent launch (narrow items, chunks of
-// at most 32 rows); the front end has zeroed the per-expert counters.
-cudaError_t run_gemms_fused(moe_layer* L, int64_t chunks, int pair, void* reduce_out,
-                            cudaStream_t s) {
+// at most 32 rows); the one-kernel front end has zeroed the per-expert
+// counters.
+cudaError_t run_gemms_fused(moe_layer* L, int64_t chunks, int max_rows, int pair,
+                            void* reduce_out, cudaStream_t s) {
   GemmArgs a1 = gemm1_args(L, pair, false);
   a1.done1 = L->done1;
   const GemmArgs a2 = gemm2_args(L, pair, false, L->y, 0, reduce_out);
   const int grid = static_cast<int>(
       std::min<int64_t>(L->num_sms, chunks * (a1.n_tiles + a2.n_tiles)));
   return launch_gemm_fused(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a1, L->maps2, a2,
-                           grid, s);
+                           grid, max_rows, s);
 }
 
 }  // namespace
@@ -456,9 +457,10 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   const int pair = L->pair_scale_copies && T <= kPairCopyMaxTokens;
   const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && T > kPairCopyMaxTokens);
   void* reduce_out = L->combine == MOE_COMBINE_REDUCE ? out : nullptr;
+  // decode: both GEMMs in one launch (for larger T the split measured faster)
   if (small && !wide && L->fused_gemms) {
     // one launch for both GEMMs (timed as GEMM1)
-    if (e == cudaSuccess) e = run_gemms_fused(L, chunks, pair, reduce_out, s);
+    if (e == cudaSuccess) e = run_gemms_fused(L, chunks, T, pair, reduce_out, s);
     --launches;
     mark(4);
   } else {

@@ -849,17 +849,33 @@ cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& 
   return launch_epi<kFmtNVFP4>(epi, maps, args, grid, max_rows, wide, s);
 }
 
+namespace {
+
+template <int FMT, int EPI>
+cudaError_t launch_fused_fmt(const GemmMaps& maps1, const GemmArgs& args1, const GemmMaps& maps2,
+                             const GemmArgs& args2, int grid, int mrows, cudaStream_t s) {
+  if (mrows > 32) return cudaErrorInvalidValue;  // decode-sized chunks only
+  return launch_one<FMT, EPI, 32, 1, true>(maps1, args1, maps2, args2, grid, s);
+}
+
+template <int FMT>
+cudaError_t launch_fused_epi(int epi1, const GemmMaps& maps1, const GemmArgs& args1,
+                             const GemmMaps& maps2, const GemmArgs& args2, int grid, int mrows,
+                             cudaStream_t s) {
+  return epi1 == 3 ? launch_fused_fmt<FMT, 3>(maps1, args1, maps2, args2, grid, mrows, s)
+                   : launch_fused_fmt<FMT, 1>(maps1, args1, maps2, args2, grid, mrows, s);
+}
+
+}  // namespace
+
 cudaError_t launch_gemm_fused(int fmt, int epi1, const GemmMaps& maps1, const GemmArgs& args1,
                               const GemmMaps& maps2, const GemmArgs& args2, int grid,
-                              cudaStream_t s) {
+                              int max_rows, cudaStream_t s) {
   if (fmt == kFmtBF16)
-    return epi1 == 3 ? launch_one<kFmtBF16, 3, 32, 1, true>(maps1, args1, maps2, args2, grid, s)
-                     : launch_one<kFmtBF16, 1, 32, 1, true>(maps1, args1, maps2, args2, grid, s);
+    return launch_fused_epi<kFmtBF16>(epi1, maps1, args1, maps2, args2, grid, max_rows, s);
   if (fmt == kFmtMXFP8)
-    return epi1 == 3 ? launch_one<kFmtMXFP8, 3, 32, 1, true>(maps1, args1, maps2, args2, grid, s)
-                     : launch_one<kFmtMXFP8, 1, 32, 1, true>(maps1, args1, maps2, args2, grid, s);
-  return epi1 == 3 ? launch_one<kFmtNVFP4, 3, 32, 1, true>(maps1, args1, maps2, args2, grid, s)
-                   : launch_one<kFmtNVFP4, 1, 32, 1, true>(maps1, args1, maps2, args2, grid, s);
+    return launch_fused_epi<kFmtMXFP8>(epi1, maps1, args1, maps2, args2, grid, max_rows, s);
+  return launch_fused_epi<kFmtNVFP4>(epi1, maps1, args1, maps2, args2, grid, max_rows, s);
 }
 
 }  // namespace moe

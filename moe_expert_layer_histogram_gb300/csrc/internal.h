@@ -120,11 +120,11 @@ cudaError_t gemm_prepare(int fmt);  // raise the dynamic shared-memory limit
 // whose chunks are mostly full 128-row blocks.
 cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& args, int grid,
                         int max_rows, bool wide, cudaStream_t s);
-// Decode (chunks of <= 32 rows, narrow items): GEMM1 (epi1 = 1 or 3) and
-// GEMM2 in one persistent launch; args1.done1 must be zero per expert.
+// Decode (chunks of at most 32 rows, narrow items): GEMM1 (epi1 = 1 or 3)
+// and GEMM2 in one persistent launch; args1.done1 must be zero per expert.
 cudaError_t launch_gemm_fused(int fmt, int epi1, const GemmMaps& maps1, const GemmArgs& args1,
                               const GemmMaps& maps2, const GemmArgs& args2, int grid,
-                              cudaStream_t s);
+                              int max_rows, cudaStream_t s);
 
 // Routing, permutation + activation quantisation, combine.
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* w,
