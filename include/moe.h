@@ -163,7 +163,10 @@ moe_status moe_forward_batched(moe_layer *layer, const void *hidden,
 /* Same as moe_forward with HOST buffers: copies hidden [T,H] bf16 and
  * router_logits [T,E] f32 to the device, runs the layer and copies out
  * [T,H] bf16 back, all on `stream`; returns once `stream` has finished
- * (synchronises it).  Errors as moe_forward.                               */
+ * (synchronises it).  When all three buffers are page-locked host memory
+ * the device can address (cudaHostAlloc / cudaHostRegister on a coherent
+ * Grace-Blackwell node), the kernels read the inputs and write the output
+ * in host memory directly instead of copying.  Errors as moe_forward.    */
 moe_status moe_forward_host(moe_layer *layer, const void *hidden_host,
                             const float *router_logits_host, void *out_host,
                             int T, void *stream);

@@ -45,6 +45,7 @@ struct moe_layer {
   int32_t *acc_cnt = nullptr, *prow_slot = nullptr;
   int32_t* done1 = nullptr;          // fused decode GEMMs: per-expert GEMM1 completion counts
   int fused_gemms = 1;               // T <= 16: GEMM1 and GEMM2 in one launch
+  int host_zero_copy = 1;            // moe_forward_host: kernels access pinned host buffers
   float* w = nullptr;
   uint8_t *xq = nullptr, *xsf = nullptr, *hq = nullptr, *hsf = nullptr, *y = nullptr;
   uint8_t *w13t = nullptr, *w2t = nullptr;  // prepared weight tiles
@@ -235,6 +236,17 @@ cudaError_t run_gemms_fused(moe_layer* L, int64_t chunks, int max_rows, int pair
                            grid, max_rows, s);
 }
 
+// The device address of page-locked host memory, or nullptr when `p` is not
+// page-locked host memory the device can address.
+void* device_view(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -329,6 +341,8 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   if (const char* tv = std::getenv("MOE_TEST_STALL_GEMM")) L->test_stall = tv[0] == '1';
   // MOE_FUSED_GEMMS=0: decode launches keep GEMM1 and GEMM2 separate.
   if (const char* fv = std::getenv("MOE_FUSED_GEMMS")) L->fused_gemms = fv[0] != '0';
+  // MOE_HOST_ZERO_COPY=0: moe_forward_host always copies through device buffers.
+  if (const char* zv = std::getenv("MOE_HOST_ZERO_COPY")) L->host_zero_copy = zv[0] != '0';
   const int H = L->H, I = L->I, E = L->E;
   if (L->fmt == MOE_FMT_NVFP4) {
     L->xb = H / 2; L->hb = I / 2; L->x_tiles_k = H / 64; L->h_tiles_k = I / 64;
@@ -512,6 +526,18 @@ moe_status moe_forward_host(moe_layer* L, const void* hidden_host, const float* 
   if (!hidden_host || !logits_host || !out_host) return MOE_ERR_INVALID_ARG;
   if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Page-locked host buffers the device can address (on a Grace-Blackwell
+  // node over NVLink-C2C) are read and written by the kernels in place: the
+  // front end reads the hidden states and logits, the combine writes the
+  // output, with no separate copies.  Other host memory is copied.
+  void* hd = L->host_zero_copy ? device_view(hidden_host) : nullptr;
+  void* ld = L->host_zero_copy ? device_view(logits_host) : nullptr;
+  void* od = L->host_zero_copy ? device_view(out_host) : nullptr;
+  if (hd && ld && od) {
+    moe_status st = moe_forward(L, hd, static_cast<const float*>(ld), od, T, stream);
+    if (st != MOE_OK) return st;
+    return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   const size_t hb = static_cast<size_t>(T) * L->H * 2, lb = static_cast<size_t>(T) * L->E * 4;
   if (cudaMemcpyAsync(L->h_in, hidden_host, hb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(L->l_in, logits_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess)

@@ -121,17 +121,32 @@ def test_out_written_in_place_and_deterministic():
     layer.close()
 
 
-def test_forward_host_matches_device_forward():
+@pytest.mark.parametrize("T", [80, 7])
+def test_forward_host_matches_device_forward(T, monkeypatch):
+    # pinned host buffers: the kernels read and write them in place; pageable
+    # buffers (and MOE_HOST_ZERO_COPY=0) go through device copies
     from moe_expert_layer_histogram_gb300 import moe_forward_host
-    s = workloads.spec("mxfp8_small")
+    s = workloads.spec("mxfp8_small", T=T)
     case = workloads.make_case(s, seed=2)
+    stream = torch.cuda.current_stream().cuda_stream
     layer = make_layer(s, weights=case["weights"])
     dev_out = run_gpu(layer, case["hidden"], case["logits"]).cpu()
     hid = case["hidden"].contiguous().pin_memory()
     lg = case["logits"].contiguous().pin_memory()
     host_out = torch.empty_like(hid).pin_memory()
-    moe_forward_host(layer.handle, hid, lg, host_out, s["T"], torch.cuda.current_stream().cuda_stream)
+    moe_forward_host(layer.handle, hid, lg, host_out, s["T"], stream)
     assert torch.equal(host_out, dev_out)
+    pageable_out = torch.empty_like(case["hidden"])
+    moe_forward_host(layer.handle, case["hidden"].contiguous(), case["logits"].contiguous(),
+                     pageable_out, s["T"], stream)
+    assert torch.equal(pageable_out, dev_out)
+    layer.close()
+    monkeypatch.setenv("MOE_HOST_ZERO_COPY", "0")
+    layer = make_layer(s, weights=case["weights"])
+    host_out.zero_()
+    moe_forward_host(layer.handle, hid, lg, host_out, s["T"], stream)
+    assert torch.equal(host_out, dev_out)
+    assert layer.status() == 0
     layer.close()
 
 
