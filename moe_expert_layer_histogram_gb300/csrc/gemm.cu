@@ -7,23 +7,26 @@
 // 16, global scale folded in); the block-scaled MMA applies both operands'
 // scales.  GEMM1's epilogue applies SwiGLU with the optional gate/up clamp
 // (or the non-gated squared ReLU) and re-quantises the result into GEMM2's
-// input format; GEMM2's epilogue stores bf16.  (The two expert GEMMs with SwiGLU between them: PR #40082
-// report, sec. 实现拆解 item 1.)
+// input format; GEMM2's epilogue stores bf16 (or, with the in-kernel
+// reduce, adds the weighted rows into an fp32 accumulator).  (The two expert
+// GEMMs with SwiGLU between them: PR #40082 report, sec. 实现拆解 item 1.)
 //
 // Structure: one persistent CTA per SM walks the device-built work list
-// (expert, 128-column weight tile, 128-row token chunk).  Warp 0 (one
-// thread) streams 128-byte K slices into a shared-memory ring (6-8 stages): the
-// activation tile by TMA (box height = the chunk's real rows, rounded up to
-// 16/32/64/128) plus its scale tiles, and the weight tile with its scales as
-// one contiguous pre-swizzled bulk copy.  Stage layout: A codes (MROWS x
-// 128 bytes), B codes (16 KiB), B scales, A scales.  The MMA always reads 128
-// A rows; rows past the region belong to the B tile and only feed
-// accumulator rows that are never stored.  Warp 1 (one thread) owns TMEM: it copies the scale
-// tiles into TMEM (tcgen05.cp) and issues 128x128 tcgen05.mma into one of two
-// 128-column fp32 accumulators.  Warps 2-5 drain the other accumulator
-// (tcgen05.ld), run the epilogue and store.  The token tile is the MMA's M
-// (128 rows; only the chunk's real rows are loaded and stored) and the weight
-// tile its N (128), so decode-sized chunks cost no extra weight traffic.
+// (expert, weight tile(s), 128-row token chunk), expert-major.  Warp 2 (one
+// thread) streams 128-byte K slices into a shared-memory ring (4-8 stages):
+// the activation tile by TMA (box height = the chunk's real rows, rounded
+// up to 16/32/64/128) plus its scale tiles, and each pre-swizzled weight
+// tile with its scales by bulk copy.  Stage layout: A codes (MROWS x 128
+// bytes), B codes (NW x 16 KiB), B scales, A scales.  The MMA always reads
+// 128 A rows; rows past the region only feed accumulator rows that are
+// never stored.  Warp 1 (one thread) owns TMEM: it copies the scale tiles
+// into TMEM (tcgen05.cp; for decode chunks warp 0 writes them with
+// tcgen05.st instead) and issues 128 x (128 NW) tcgen05.mma into an fp32
+// accumulator (two of 128 columns, or one of 256 for wide items).  Warps 3..
+// drain it (tcgen05.ld), run the epilogue and store.  The token tile is the
+// MMA's M (only the chunk's real rows are loaded and stored) and the weight
+// tile its N, so decode-sized chunks cost no extra weight traffic.  Decode
+// launches (T <= 16) run GEMM1 and GEMM2 in one persistent launch (FUSED).
 #include <cuda_bf16.h>
 
 #include "internal.h"
