@@ -165,20 +165,29 @@ def algorithmic_bytes(s, counts):
     return {"gemm1_swiglu": g1, "gemm2": g2}, touched
 
 
+def source_digest(path):
+    """SHA-1 of a C++/CUDA source with comments and whitespace removed, so
+    that edits of comments alone do not mark a capture as stale."""
+    import hashlib
+    import re
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha1(" ".join(text.split()).encode()).hexdigest()
+
+
 def ncu_traffic(s, touched, kernel):
     """DRAM bytes per launch of `kernel` from the committed ncu captures
     (profiles/gemm_traffic.json), scaled from the captured case to this run
     by the number of touched experts (the weights dominate the traffic).
     None when the workload was not captured or the kernel sources changed
     since the capture."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
     try:
         tab = json.load(open(path))
         for src, digest in tab["sources_sha1"].items():
-            with open(os.path.join(ROOT, src), "rb") as f:
-                if hashlib.sha1(f.read()).hexdigest() != digest:
-                    return None, "kernel changed since the ncu capture"
+            if source_digest(os.path.join(ROOT, src)) != digest:
+                return None, "kernel changed since the ncu capture"
         per = tab["per_touched_expert_bytes"][s["name"]][kernel]
     except (OSError, KeyError, ValueError):
         return None, "no ncu capture for this workload and kernel"
