@@ -353,7 +353,9 @@ def test_batched_capacity_and_arguments():
     ("nvfp4_small", dict(act="relu2"), True),
     ("mxfp8_small", dict(act="relu2", T=150, E=4, K=2), True),
     ("nvfp4_zipf_small", dict(T=1100, E=24, K=4), False),   # T > 1024 selects them itself
-], ids=["bf16", "mxfp8", "nvfp4", "nvfp4-chunks", "nvfp4-relu2", "mxfp8-relu2", "nvfp4-T1100"])
+    ("nvfp4_zipf_small", dict(T=2100, E=24, K=4), False),   # and the two-pass expert scan
+], ids=["bf16", "mxfp8", "nvfp4", "nvfp4-chunks", "nvfp4-relu2", "mxfp8-relu2", "nvfp4-T1100",
+        "nvfp4-T2100"])
 def test_wide_items_match_oracle(name, over, force, monkeypatch):
     if force:
         monkeypatch.setenv("MOE_WIDE_TILES", "1")
@@ -418,4 +420,39 @@ def test_in_kernel_reduce_matches_oracle(name, over, wide, monkeypatch):
         assert rel_l2(o, bf16_bits_to_f64(ref["out"])) <= TOL[s["fmt"]]
     # only the summation order differs between runs: last-bit differences at most
     assert max(np.max(np.abs(o - outs[0])) for o in outs) <= 1e-2 * np.max(np.abs(outs[0]))
+    layer.close()
+
+
+@pytest.mark.parametrize("T", [9, 40])
+def test_top16_routing_matches_oracle(T):
+    # K = 16, the largest top-k the library accepts (one-kernel front end for
+    # T <= 16, the three-kernel one above)
+    s = workloads.spec("nvfp4_small", T=T, E=40, K=16)
+    case = workloads.make_case(s, seed=29)
+    ref = run_oracle(s, case)
+    layer = make_layer(s, weights=case["weights"])
+    out = run_gpu(layer, case["hidden"], case["logits"])
+    ids, w, off, perm = (t.cpu().numpy() for t in layer.routing())
+    assert np.array_equal(ids, ref["ids"]) and np.array_equal(off, ref["offsets"])
+    assert np.array_equal(perm, ref["perm"])
+    assert rel_l2(out.float().cpu().numpy(), bf16_bits_to_f64(ref["out"])) <= TOL["nvfp4"]
+    assert layer.status() == 0
+    layer.close()
+
+
+def test_forward_on_a_side_stream():
+    # work is enqueued on the caller's stream only; results match the default
+    # stream's bit for bit
+    s = workloads.spec("mxfp8_small")
+    case = workloads.make_case(s, seed=31)
+    layer = make_layer(s, weights=case["weights"])
+    ref = run_gpu(layer, case["hidden"], case["logits"]).clone()
+    side = torch.cuda.Stream()
+    hid, lg = case["hidden"].cuda(), case["logits"].cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        out = layer.forward(hid, lg)
+        side.synchronize()
+    assert torch.equal(out, ref)
+    assert layer.status() == 0
     layer.close()
