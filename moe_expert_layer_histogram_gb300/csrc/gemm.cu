@@ -46,8 +46,10 @@ constexpr int kTmemCols = 512;
 // the main loop of the next) and 32 scale columns per stage.  NW = 2 (wide
 // items, N = 256: half the shared-memory traffic per FLOP for the
 // activation operand): one 256-column accumulator and 64 scale columns per
-// stage (activation tile j at 16 j, weight tiles j at 16 j + 8 and
-// 16 j + 12 for NVFP4; MXFP8: weight tiles at 0 and 4, activation at 8).
+// stage (MXFP8: weight tiles at 0 and 4, activation at 8; NVFP4 copied by
+// the MMA thread: activation tile j at 16 j, weight tiles j at 16 j + 8 and
+// 16 j + 12; NVFP4 written by the scale-stager warps: weight tiles j at 8 j
+// and 8 j + 4, activation rows of lane quarter q at column 32 + 4 j + q).
 template <int NW>
 struct Wide {
   static constexpr int kAccCols = 128 * NW;       // TMEM columns per accumulator
@@ -108,7 +110,23 @@ __host__ __device__ constexpr int smem_bytes() {
 
 // Warp 0 stages decode scales into TMEM lane quarter 0, warp 1 issues the
 // MMAs, warp 2 the copies, then four epilogue warps per 128-column group.
-__host__ __device__ constexpr int gemm_threads(int nw) { return 96 + 128 * nw; }
+// Wide NVFP4 items add four scale-stager warps (warps 12-15, one per TMEM
+// lane quarter) and start the epilogue warps at warp 4, so that every
+// warpgroup has one role and one register budget: warps 0-3 and 12-15 keep
+// kLeanRegs registers, the epilogue warpgroups (which hold a 128-column
+// accumulator slice in registers) kEpiRegs.
+__host__ __device__ constexpr bool wide_stager(int fmt, int nw) {
+  return fmt == kFmtNVFP4 && nw == 2;
+}
+__host__ __device__ constexpr int gemm_threads(int fmt, int nw) {
+  return wide_stager(fmt, nw) ? 512 : 96 + 128 * nw;
+}
+constexpr int kEpiRegs = 176;
+constexpr int kLeanRegs = 80;
+// registers per thread the 512-thread block must be launched with for the
+// split to balance: 2 x 128 threads give up (R - 80), 256 claim (176 - R)
+constexpr int kSplitLaunchRegs = (2 * kLeanRegs + 2 * kEpiRegs) / 4;
+static_assert(kSplitLaunchRegs * 512 <= 65536, "register split exceeds the register file");
 
 struct Item {
   int e, n_tile, prow0, rows;
@@ -365,7 +383,7 @@ __device__ __forceinline__ void epilogue_round(const uint32_t* v, int p, bool st
 // each epilogue warp.  CTAs whose GEMM1 share ends early move on to GEMM2
 // work instead of idling until the slowest CTA finishes.
 template <int FMT, int EPI, int MROWS, int NW, bool FUSED>
-__global__ void __launch_bounds__(gemm_threads(NW), 1)
+__global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs args,
                     const __grid_constant__ GemmMaps maps2,
                     const __grid_constant__ GemmArgs args2) {
@@ -376,6 +394,8 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
   constexpr int kAccCols = Wide<NW>::kAccCols;
   constexpr int kBufs = Wide<NW>::kBufs;
   constexpr int kSfColsPerStage = Wide<NW>::kSfCols;
+  constexpr bool WS = wide_stager(FMT, NW);
+  constexpr int kEpiWarp0 = WS ? 4 : 3;  // first epilogue warp
   // shared-memory offsets inside a stage
   constexpr int kOffBsf = A_BYTES + NW * kTileBytes;        // weight scale tiles
   constexpr int kOffAsf = kOffBsf + NW * SFT * 512;          // activation scale tiles
@@ -398,7 +418,7 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_ready[s], 1);
+      mbar_init(&sf_ready[s], WS ? 4 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -440,280 +460,361 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
   // tensor pipe; every stage of such a launch then reaches the MMA through
   // warp 0's sf_ready barrier.
   const bool staged = NW == 1 && SFT > 0 && args.pair_scale_copies && args.stage_scales;
+  // Wide NVFP4 items: warps 12-15 write every stage's scales into their lane
+  // quarters with tcgen05.st (the activation scales of quarter q in one
+  // column per 64-element substep, the weight scales replicated in every
+  // quarter) instead of the MMA thread broadcasting twelve tiles with
+  // tcgen05.cp; the copies queue in order with the MMAs on the tensor pipe.
+  // GEMM2 keeps the copies: its short items mostly stream weights from HBM,
+  // and the stagers' hop between a stage landing and its MMAs holds ring
+  // slots longer, which costs more bandwidth than the copies cost MMA time.
+  const bool wstaged = WS && EPI != 2 && args.stage_scales;
 
-  if (warp == 0) {
-    // ------------------------------------------------ scale stager
-    if (staged) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const GemmArgs& A = gargs(item);
-        const bool q0 = map_item(tab, args.E, A.n_tiles, local_item(item)).rows <= 32;
-        for (int kb = 0; kb < A.num_kb; ++kb) {
-          const bool landed = mbar_wait(&full[stage], phase, abort_flag);
-          if (!__all_sync(0xFFFFFFFFu, landed)) {
-            ok = false;
-            break;
-          }
-          if (q0) {
-            const uint8_t* sp = smem + stage * SB;
-            const uint32_t col = tmem + kSfColBase + stage * kSfColsPerStage;  // lanes 0-31
-            if constexpr (FMT == kFmtNVFP4) {
-              // per 64-element substep j: activation row (lane) scales in
-              // column 8j, the 128 weight rows' scales in columns 8j+4..8j+7
-              uint32_t v[32];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const uint4 b = *reinterpret_cast<const uint4*>(sp + kOffBsf + j * 512 + lane * 16);
-                v[8 * j] = *reinterpret_cast<const uint32_t*>(sp + kOffAsf + j * 512 + lane * 16);
-                v[8 * j + 1] = v[8 * j + 2] = v[8 * j + 3] = 0u;
-                v[8 * j + 4] = b.x;
-                v[8 * j + 5] = b.y;
-                v[8 * j + 6] = b.z;
-                v[8 * j + 7] = b.w;
-              }
-              tmem_st32(col, v);
-            } else {
-              // weight rows' scales in columns 0-3, activation row in 4
-              uint32_t v[8];
-              const uint4 b = *reinterpret_cast<const uint4*>(sp + kOffBsf + lane * 16);
-              v[0] = b.x;
-              v[1] = b.y;
-              v[2] = b.z;
-              v[3] = b.w;
-              v[4] = *reinterpret_cast<const uint32_t*>(sp + kOffAsf + lane * 16);
-              v[5] = v[6] = v[7] = 0u;
-              tmem_st8(col, v);
+  // Roles by warpgroup: a warpgroup's register budget changes at the top of
+  // its branch, before any of its roles' code.
+  const bool epi_warp = warp >= kEpiWarp0 && warp < kEpiWarp0 + 4 * NW;
+  if (!epi_warp) {
+    if constexpr (WS) regs_release<kLeanRegs>();
+    if (warp == 0) {
+      // ------------------------------------------------ scale stager
+      if (staged) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+          const GemmArgs& A = gargs(item);
+          const bool q0 = map_item(tab, args.E, A.n_tiles, local_item(item)).rows <= 32;
+          for (int kb = 0; kb < A.num_kb; ++kb) {
+            const bool landed = mbar_wait(&full[stage], phase, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, landed)) {
+              ok = false;
+              break;
             }
-            tmem_st_wait();
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sf_ready[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok && lane == 0) report_status(args.status, kStatusTimeout);
-    }
-  } else if (warp == 2) {
-    // ------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t policy = l2_policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0;
-      int slots = 0;          // ring positions used so far
-      int skipped = -1;       // position the test hook left unloaded
-      bool ok = true;
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const GemmArgs& A = gargs(item);
-        const CUtensorMap* amaps = second(item) ? maps2.a : maps.a;
-        const Item it = map_item(tab, args.E, A.n_tiles, local_item(item));
-        const int amap = it.rows <= 16 ? 0 : it.rows <= 32 ? 1 : it.rows <= 64 ? 2 : 3;
-        if ((16 << amap) > MROWS) {   // the host bounded the rows per chunk by MROWS
-          ok = false;
-          break;
-        }
-        if (second(item)) {
-          // GEMM2's activations are GEMM1's output for this expert
-          const int need = 4 * args.n_tiles * (tab.chunk_off[it.e + 1] - tab.chunk_off[it.e]);
-          if (!wait_count_at_least(args.done1 + it.e, need, abort_flag)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async_global();  // generic-proxy stores -> the TMA reads below
-        }
-        const uint32_t bytes = (16u << amap) * 128u + NW * A.b_tile_bytes + SFT * 512u;
-        const uint8_t* sfa = A.sfa + static_cast<int64_t>(it.prow0 >> 7) * A.sfa_tiles_k * 512;
-        // the item's first 128-row weight tile; the next one (NW = 2)
-        // follows num_kb tiles later
-        const uint8_t* btile =
-            A.b_tiles + (static_cast<int64_t>(it.e) * A.n_tiles + it.n_tile) * NW * A.num_kb *
-                            A.b_tile_bytes;
-        for (int kb = 0; kb < A.num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (A.test_stall && blockIdx.x == 0 && skipped < 0) {
-            // test hook: nothing ever completes this stage
-            skipped = slots++;
+            if (q0) {
+              const uint8_t* sp = smem + stage * SB;
+              const uint32_t col = tmem + kSfColBase + stage * kSfColsPerStage;  // lanes 0-31
+              if constexpr (FMT == kFmtNVFP4) {
+                // per 64-element substep j: activation row (lane) scales in
+                // column 8j, the 128 weight rows' scales in columns 8j+4..8j+7
+                uint32_t v[32];
+  #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const uint4 b = *reinterpret_cast<const uint4*>(sp + kOffBsf + j * 512 + lane * 16);
+                  v[8 * j] = *reinterpret_cast<const uint32_t*>(sp + kOffAsf + j * 512 + lane * 16);
+                  v[8 * j + 1] = v[8 * j + 2] = v[8 * j + 3] = 0u;
+                  v[8 * j + 4] = b.x;
+                  v[8 * j + 5] = b.y;
+                  v[8 * j + 6] = b.z;
+                  v[8 * j + 7] = b.w;
+                }
+                tmem_st32(col, v);
+              } else {
+                // weight rows' scales in columns 0-3, activation row in 4
+                uint32_t v[8];
+                const uint4 b = *reinterpret_cast<const uint4*>(sp + kOffBsf + lane * 16);
+                v[0] = b.x;
+                v[1] = b.y;
+                v[2] = b.z;
+                v[3] = b.w;
+                v[4] = *reinterpret_cast<const uint32_t*>(sp + kOffAsf + lane * 16);
+                v[5] = v[6] = v[7] = 0u;
+                tmem_st8(col, v);
+              }
+              tmem_st_wait();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sf_ready[stage]);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
-            continue;
           }
-          uint8_t* sp = smem + stage * SB;
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(sp, &amaps[amap], &full[stage], kb * 128, it.prow0);
-          if constexpr (NW == 1) {
-            // weight tile codes + its scale tiles: one contiguous block
-            bulk_load_hint(sp + A_BYTES, btile + static_cast<int64_t>(kb) * A.b_tile_bytes,
-                           A.b_tile_bytes, &full[stage], policy);
-          } else {
-            // codes of both tiles back to back (one 256-row operand), then
-            // their scale tiles
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-              const uint8_t* src =
-                  btile + (static_cast<int64_t>(w) * A.num_kb + kb) * A.b_tile_bytes;
-              bulk_load_hint(sp + A_BYTES + w * kTileBytes, src, kTileBytes, &full[stage], policy);
-              if constexpr (SFT > 0)
-                bulk_load_hint(sp + kOffBsf + w * SFT * 512, src + kTileBytes, SFT * 512,
-                               &full[stage], policy);
+        }
+        if (!ok && lane == 0) report_status(args.status, kStatusTimeout);
+      }
+    } else if (warp == 2) {
+      // ------------------------------------------------ TMA producer
+      if (lane == 0) {
+        const uint64_t policy = l2_policy_evict_first();
+        int stage = 0;
+        uint32_t phase = 0;
+        int slots = 0;          // ring positions used so far
+        int skipped = -1;       // position the test hook left unloaded
+        bool ok = true;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+          const GemmArgs& A = gargs(item);
+          const CUtensorMap* amaps = second(item) ? maps2.a : maps.a;
+          const Item it = map_item(tab, args.E, A.n_tiles, local_item(item));
+          const int amap = it.rows <= 16 ? 0 : it.rows <= 32 ? 1 : it.rows <= 64 ? 2 : 3;
+          if ((16 << amap) > MROWS) {   // the host bounded the rows per chunk by MROWS
+            ok = false;
+            break;
+          }
+          if (second(item)) {
+            // GEMM2's activations are GEMM1's output for this expert
+            const int need = 4 * args.n_tiles * (tab.chunk_off[it.e + 1] - tab.chunk_off[it.e]);
+            if (!wait_count_at_least(args.done1 + it.e, need, abort_flag)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_global();  // generic-proxy stores -> the TMA reads below
+          }
+          const uint32_t bytes = (16u << amap) * 128u + NW * A.b_tile_bytes + SFT * 512u;
+          const uint8_t* sfa = A.sfa + static_cast<int64_t>(it.prow0 >> 7) * A.sfa_tiles_k * 512;
+          // the item's first 128-row weight tile; the next one (NW = 2)
+          // follows num_kb tiles later
+          const uint8_t* btile =
+              A.b_tiles + (static_cast<int64_t>(it.e) * A.n_tiles + it.n_tile) * NW * A.num_kb *
+                              A.b_tile_bytes;
+          for (int kb = 0; kb < A.num_kb; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (A.test_stall && blockIdx.x == 0 && skipped < 0) {
+              // test hook: nothing ever completes this stage
+              skipped = slots++;
+              if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+              }
+              continue;
+            }
+            uint8_t* sp = smem + stage * SB;
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            tma_load_2d(sp, &amaps[amap], &full[stage], kb * 128, it.prow0);
+            if constexpr (NW == 1) {
+              // weight tile codes + its scale tiles: one contiguous block
+              bulk_load_hint(sp + A_BYTES, btile + static_cast<int64_t>(kb) * A.b_tile_bytes,
+                             A.b_tile_bytes, &full[stage], policy);
+            } else {
+              // codes of both tiles back to back (one 256-row operand), then
+              // their scale tiles
+  #pragma unroll
+              for (int w = 0; w < NW; ++w) {
+                const uint8_t* src =
+                    btile + (static_cast<int64_t>(w) * A.num_kb + kb) * A.b_tile_bytes;
+                bulk_load_hint(sp + A_BYTES + w * kTileBytes, src, kTileBytes, &full[stage], policy);
+                if constexpr (SFT > 0)
+                  bulk_load_hint(sp + kOffBsf + w * SFT * 512, src + kTileBytes, SFT * 512,
+                                 &full[stage], policy);
+              }
+            }
+            if constexpr (SFT > 0)
+              bulk_load(sp + kOffAsf, sfa + kb * SFT * 512, SFT * 512, &full[stage]);
+            ++slots;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
             }
           }
-          if constexpr (SFT > 0)
-            bulk_load(sp + kOffAsf, sfa + kb * SFT * 512, SFT * 512, &full[stage]);
-          ++slots;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
-      }
-      // Before leaving, make sure no copy this thread issued is still in
-      // flight (they all completed already unless the block gave up).
-      for (int back = 1; back <= kStages && back <= slots; ++back) {
-        const int idx = slots - back;
-        if (idx == skipped) continue;
-        mbar_wait(&full[idx % kStages], static_cast<uint32_t>((idx / kStages) & 1), nullptr);
-      }
-      if (!ok) report_status(args.status, kStatusTimeout);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t idesc;
-      if constexpr (FMT == kFmtBF16) idesc = idesc_bf16(128, 128 * NW);
-      else if constexpr (FMT == kFmtNVFP4) idesc = idesc_nvf4(128, 128 * NW);
-      else idesc = 0;
-      int stage = 0;
-      uint32_t phase = 0;
-      int local = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++local) {
-        const GemmArgs& A = gargs(item);
-        const int buf = local % kBufs;
-        const uint32_t use = static_cast<uint32_t>(local / kBufs);
-        // A chunk of at most 32 rows keeps all its real accumulator rows in
-        // TMEM lane quarter 0.  The MMA of each lane quarter reads both
-        // operands' scales from that quarter's own lanes, so then only lanes
-        // 0-31 need correct scales: two 512-byte scale tiles go in with one
-        // non-broadcast 128x256b copy (the other lanes receive neighbouring
-        // shared memory and only feed accumulator rows that are not stored).
-        // Larger chunks broadcast every tile to all four quarters.
-        const bool q0_only = NW == 1 && args.pair_scale_copies &&
-                             map_item(tab, args.E, A.n_tiles, local_item(item)).rows <= 32;
-        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
-          ok = false;
-          break;
+        // Before leaving, make sure no copy this thread issued is still in
+        // flight (they all completed already unless the block gave up).
+        for (int back = 1; back <= kStages && back <= slots; ++back) {
+          const int idx = slots - back;
+          if (idx == skipped) continue;
+          mbar_wait(&full[idx % kStages], static_cast<uint32_t>((idx / kStages) & 1), nullptr);
         }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * kAccCols;
-        for (int kb = 0; kb < A.num_kb; ++kb) {
-          if (!mbar_wait(staged ? &sf_ready[stage] : &full[stage], phase, abort_flag)) {
+        if (!ok) report_status(args.status, kStatusTimeout);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        uint32_t idesc;
+        if constexpr (FMT == kFmtBF16) idesc = idesc_bf16(128, 128 * NW);
+        else if constexpr (FMT == kFmtNVFP4) idesc = idesc_nvf4(128, 128 * NW);
+        else idesc = 0;
+        int stage = 0;
+        uint32_t phase = 0;
+        int local = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++local) {
+          const GemmArgs& A = gargs(item);
+          const int buf = local % kBufs;
+          const uint32_t use = static_cast<uint32_t>(local / kBufs);
+          // A chunk of at most 32 rows keeps all its real accumulator rows in
+          // TMEM lane quarter 0.  The MMA of each lane quarter reads both
+          // operands' scales from that quarter's own lanes, so then only lanes
+          // 0-31 need correct scales: two 512-byte scale tiles go in with one
+          // non-broadcast 128x256b copy (the other lanes receive neighbouring
+          // shared memory and only feed accumulator rows that are not stored).
+          // Larger chunks broadcast every tile to all four quarters.
+          const bool q0_only = NW == 1 && args.pair_scale_copies &&
+                               map_item(tab, args.E, A.n_tiles, local_item(item)).rows <= 32;
+          if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          uint8_t* sp = smem + stage * SB;
-          const uint32_t a_addr = smem_u32(sp), b_addr = smem_u32(sp + A_BYTES);
-          uint8_t* sf = sp + kOffBsf;  // weight scales, then activation scales
-          const uint32_t sf_col = tmem + kSfColBase + stage * kSfColsPerStage;
-          if constexpr (FMT == kFmtNVFP4 && NW == 2) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tc_copy_sf(sf_col + j * 16, desc_sf(smem_u32(sp + kOffAsf + j * 512)));
-              tc_copy_sf(sf_col + j * 16 + 8, desc_sf(smem_u32(sf + j * 512)));
-              tc_copy_sf(sf_col + j * 16 + 12, desc_sf(smem_u32(sf + (SFT + j) * 512)));
+          const uint32_t d_tmem = tmem + buf * kAccCols;
+          for (int kb = 0; kb < A.num_kb; ++kb) {
+            if (!mbar_wait(staged || wstaged ? &sf_ready[stage] : &full[stage], phase,
+                           abort_flag)) {
+              ok = false;
+              break;
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
-                       sf_col + j * 16, sf_col + j * 16 + 8, (kb | j) != 0);
-          } else if constexpr (FMT == kFmtMXFP8 && NW == 2) {
-            tc_copy_sf(sf_col, desc_sf(smem_u32(sf)));
-            tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf + 512)));
-            tc_copy_sf(sf_col + 8, desc_sf(smem_u32(sp + kOffAsf)));
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
-                       idesc_mxf8(128, 256, j), sf_col + 8, sf_col, (kb | j) != 0);
-          } else if constexpr (FMT == kFmtNVFP4) {
-            if (q0_only && staged) {
-              // lanes 0-31 of the stage's scale columns were written by warp 0
-#pragma unroll
+            tc_fence_after();
+            uint8_t* sp = smem + stage * SB;
+            const uint32_t a_addr = smem_u32(sp), b_addr = smem_u32(sp + A_BYTES);
+            uint8_t* sf = sp + kOffBsf;  // weight scales, then activation scales
+            const uint32_t sf_col = tmem + kSfColBase + stage * kSfColsPerStage;
+            if constexpr (FMT == kFmtNVFP4 && NW == 2) {
+              if (wstaged) {
+                // the stager warps wrote this stage's scale columns
+  #pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                           sf_col + 32 + j * 4, sf_col + j * 8, (kb | j) != 0);
+              } else {
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                tc_copy_sf(sf_col + j * 16, desc_sf(smem_u32(sp + kOffAsf + j * 512)));
+                tc_copy_sf(sf_col + j * 16 + 8, desc_sf(smem_u32(sf + j * 512)));
+                tc_copy_sf(sf_col + j * 16 + 12, desc_sf(smem_u32(sf + (SFT + j) * 512)));
+              }
+  #pragma unroll
               for (int j = 0; j < 4; ++j)
                 mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
-                         sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
-            } else if (q0_only) {
-              // columns: A scales of substeps 0-1 | 2-3, B scales 0-1 | 2-3
-              const uint32_t sfa = smem_u32(sf + 4 * 512), sfb = smem_u32(sf);
-              tc_copy_128x256b(sf_col, desc_sf_pair(sfa, 512));
-              tc_copy_128x256b(sf_col + 8, desc_sf_pair(sfa + 1024, 512));
-              tc_copy_128x256b(sf_col + 16, desc_sf_pair(sfb, 512));
-              tc_copy_128x256b(sf_col + 24, desc_sf_pair(sfb + 1024, 512));
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const uint32_t c = (j >> 1) * 8 + (j & 1) * 4;
-                mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
-                         sf_col + c, sf_col + 16 + c, (kb | j) != 0);
+                         sf_col + j * 16, sf_col + j * 16 + 8, (kb | j) != 0);
               }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                tc_copy_sf(sf_col + j * 8, desc_sf(smem_u32(sf + (4 + j) * 512)));
-                tc_copy_sf(sf_col + j * 8 + 4, desc_sf(smem_u32(sf + j * 512)));
-              }
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
-                         sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
-            }
-          } else if constexpr (FMT == kFmtMXFP8) {
-            if (q0_only && staged) {
-              // lanes 0-31 of the stage's scale columns were written by warp 0
-            } else if (q0_only) {
-              // columns 0-3: B scales, 4-7: A scales (tiles adjacent in smem)
-              tc_copy_128x256b(sf_col, desc_sf_pair(smem_u32(sf), 512));
-            } else {
+            } else if constexpr (FMT == kFmtMXFP8 && NW == 2) {
               tc_copy_sf(sf_col, desc_sf(smem_u32(sf)));
               tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf + 512)));
+              tc_copy_sf(sf_col + 8, desc_sf(smem_u32(sp + kOffAsf)));
+  #pragma unroll
+              for (int j = 0; j < 4; ++j)
+                mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
+                         idesc_mxf8(128, 256, j), sf_col + 8, sf_col, (kb | j) != 0);
+            } else if constexpr (FMT == kFmtNVFP4) {
+              if (q0_only && staged) {
+                // lanes 0-31 of the stage's scale columns were written by warp 0
+  #pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                           sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
+              } else if (q0_only) {
+                // columns: A scales of substeps 0-1 | 2-3, B scales 0-1 | 2-3
+                const uint32_t sfa = smem_u32(sf + 4 * 512), sfb = smem_u32(sf);
+                tc_copy_128x256b(sf_col, desc_sf_pair(sfa, 512));
+                tc_copy_128x256b(sf_col + 8, desc_sf_pair(sfa + 1024, 512));
+                tc_copy_128x256b(sf_col + 16, desc_sf_pair(sfb, 512));
+                tc_copy_128x256b(sf_col + 24, desc_sf_pair(sfb + 1024, 512));
+  #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const uint32_t c = (j >> 1) * 8 + (j & 1) * 4;
+                  mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                           sf_col + c, sf_col + 16 + c, (kb | j) != 0);
+                }
+              } else {
+  #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  tc_copy_sf(sf_col + j * 8, desc_sf(smem_u32(sf + (4 + j) * 512)));
+                  tc_copy_sf(sf_col + j * 8 + 4, desc_sf(smem_u32(sf + j * 512)));
+                }
+  #pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                           sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
+              }
+            } else if constexpr (FMT == kFmtMXFP8) {
+              if (q0_only && staged) {
+                // lanes 0-31 of the stage's scale columns were written by warp 0
+              } else if (q0_only) {
+                // columns 0-3: B scales, 4-7: A scales (tiles adjacent in smem)
+                tc_copy_128x256b(sf_col, desc_sf_pair(smem_u32(sf), 512));
+              } else {
+                tc_copy_sf(sf_col, desc_sf(smem_u32(sf)));
+                tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf + 512)));
+              }
+  #pragma unroll
+              for (int j = 0; j < 4; ++j)
+                mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
+                         idesc_mxf8(128, 128, j), sf_col + 4, sf_col, (kb | j) != 0);
+            } else {
+  #pragma unroll
+              for (int j = 0; j < 4; ++j)
+                mma_bf16(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
+                         (kb | j) != 0);
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
-                       idesc_mxf8(128, 128, j), sf_col + 4, sf_col, (kb | j) != 0);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              mma_bf16(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
-                       (kb | j) != 0);
+            tc_commit(&empty[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          tc_commit(&empty[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+          if (ok) tc_commit(&tfull[buf]);
+        }
+        // Every MMA this thread issued must finish before TMEM is released.
+        tc_commit(drained);
+        mbar_wait(drained, 0, nullptr);
+        if (!ok) report_status(args.status, kStatusTimeout);
+      }
+    } else if (WS && warp >= kEpiWarp0 + 4 * NW) {
+      // ------------------------------------------------ wide scale stagers
+      // Warp w writes TMEM lane quarter q = w % 4 of each stage's 64 scale
+      // columns: per 64-element substep j, the 256 weight rows' scales in
+      // columns 8j..8j+7 (row n at column 8j + n/32, lane n % 32: every quarter
+      // holds all of them), and its own 32 activation rows' scales in column
+      // 32 + 4j + q (the MMA of quarter q reads column q of the four starting
+      // at the activation scale address).
+      if (wstaged) {
+        const int q = warp & 3;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+          const GemmArgs& A = gargs(item);
+          for (int kb = 0; kb < A.num_kb; ++kb) {
+            const bool landed = mbar_wait(&full[stage], phase, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, landed)) {
+              ok = false;
+              break;
+            }
+            const uint8_t* sp = smem + stage * SB;
+            uint32_t v[32];
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 b0 = *reinterpret_cast<const uint4*>(sp + kOffBsf + j * 512 + lane * 16);
+              const uint4 b1 =
+                  *reinterpret_cast<const uint4*>(sp + kOffBsf + (SFT + j) * 512 + lane * 16);
+              v[8 * j + 0] = b0.x;
+              v[8 * j + 1] = b0.y;
+              v[8 * j + 2] = b0.z;
+              v[8 * j + 3] = b0.w;
+              v[8 * j + 4] = b1.x;
+              v[8 * j + 5] = b1.y;
+              v[8 * j + 6] = b1.z;
+              v[8 * j + 7] = b1.w;
+            }
+            const uint32_t col = tmem + (static_cast<uint32_t>(q * 32) << 16) + kSfColBase +
+                                 stage * kSfColsPerStage;
+            tmem_st32(col, v);
+  #pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tmem_st1(col + 32 + 4 * j + q, *reinterpret_cast<const uint32_t*>(
+                                                 sp + kOffAsf + j * 512 + lane * 16 + q * 4));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sf_ready[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
-        if (ok) tc_commit(&tfull[buf]);
+        if (!ok && lane == 0) report_status(args.status, kStatusTimeout);
       }
-      // Every MMA this thread issued must finish before TMEM is released.
-      tc_commit(drained);
-      mbar_wait(drained, 0, nullptr);
-      if (!ok) report_status(args.status, kStatusTimeout);
     }
   } else {
-    // ------------------------------------------------ epilogue warps 3..
+    if constexpr (WS) regs_claim<kEpiRegs>();
+    // ------------------------------------------------ epilogue warps
     // Warp w reads TMEM lane quarter w % 4 (rows 32q..) of accumulator
     // column group (w - 3) / 4 (one 128-column group per weight tile).
     const int q = warp & 3;
-    const int grp = (warp - 3) >> 2;
+    const int grp = (warp - kEpiWarp0) >> 2;
     int local = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++local) {
       const GemmArgs& A = gargs(item);
@@ -786,19 +887,40 @@ __global__ void __launch_bounds__(gemm_threads(NW), 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Set once the launch allocation of a wide-stager instantiation has been
+// checked against its register split.
+template <int FMT, int EPI, int MROWS, int NW, bool FUSED>
+bool& split_checked() {
+  static bool ok = false;
+  return ok;
+}
+
 template <int FMT, int EPI, int MROWS, int NW, bool FUSED = false>
 cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, const GemmMaps& maps2,
                        const GemmArgs& args2, int grid, cudaStream_t s) {
+  if (wide_stager(FMT, NW) && !split_checked<FMT, EPI, MROWS, NW, FUSED>())
+    return cudaErrorInvalidConfiguration;
   return launch_pdl(g_pdl_gemm, moe_gemm_kernel<FMT, EPI, MROWS, NW, FUSED>, dim3(grid),
-                    dim3(gemm_threads(NW)), smem_bytes<FMT, MROWS, NW>(), s, maps, args, maps2,
-                    args2);
+                    dim3(gemm_threads(FMT, NW)), smem_bytes<FMT, MROWS, NW>(), s, maps, args,
+                    maps2, args2);
 }
 
 template <int FMT, int EPI, int MROWS, int NW, bool FUSED = false>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(moe_gemm_kernel<FMT, EPI, MROWS, NW, FUSED>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem_bytes<FMT, MROWS, NW>());
+  cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<FMT, EPI, MROWS, NW, FUSED>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes<FMT, MROWS, NW>());
+  if (e != cudaSuccess || !wide_stager(FMT, NW)) return e;
+  // The kernel's register split only balances at kSplitLaunchRegs registers
+  // per thread; with fewer, the claiming warpgroups would wait forever.
+  cudaFuncAttributes fa{};
+  e = cudaFuncGetAttributes(&fa, moe_gemm_kernel<FMT, EPI, MROWS, NW, FUSED>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kSplitLaunchRegs ||
+      fa.numRegs * gemm_threads(FMT, NW) > 65536)
+    return cudaErrorInvalidConfiguration;
+  split_checked<FMT, EPI, MROWS, NW, FUSED>() = true;
+  return cudaSuccess;
 }
 
 template <int FMT, int MROWS, int NW>
