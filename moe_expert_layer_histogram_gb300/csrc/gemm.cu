@@ -314,7 +314,25 @@ __device__ __forceinline__ void epilogue_relu2(const uint32_t* v, int p, bool st
 __device__ __forceinline__ void epilogue_gemm2(const uint32_t* v, int p, bool store, int64_t prow,
                                                int n_tile, const GemmArgs& a) {
   if (!store) return;
-  uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 256 + p * 128);
+  uint8_t* row = a.out + prow * a.out_ld + n_tile * 256 + p * 128;
+  if (((reinterpret_cast<uintptr_t>(a.out) | static_cast<uintptr_t>(a.out_ld)) & 31) == 0) {
+    // each thread owns one row: whole 32-byte sectors halve the store
+    // requests and the L2 sector writes of 16-byte stores
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t* w = v + 16 * q;
+      st_global_v8(row + 32 * q, pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                   pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                   pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                   pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])),
+                   pack_bf16x2(__uint_as_float(w[8]), __uint_as_float(w[9])),
+                   pack_bf16x2(__uint_as_float(w[10]), __uint_as_float(w[11])),
+                   pack_bf16x2(__uint_as_float(w[12]), __uint_as_float(w[13])),
+                   pack_bf16x2(__uint_as_float(w[14]), __uint_as_float(w[15])));
+    }
+    return;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(row);
 #pragma unroll
   for (int q = 0; q < 8; ++q)
     dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
