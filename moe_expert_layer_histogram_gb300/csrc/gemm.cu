@@ -207,20 +207,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 }
 
 // 16 bf16 values (32 bytes) to dst.
+// Each epilogue thread owns one row, so the lanes of a warp store to 32
+// different rows: whole 32-byte sectors per store (dst 32-byte aligned; all
+// GEMM1 outputs are layer buffers with 32-byte aligned rows) halve the
+// requests and L2 sector writes of 16-byte stores.
+__device__ __forceinline__ void store32(uint8_t* dst, const uint32_t* w) {
+  st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+}
+
 __device__ __forceinline__ void store_bf16x16(uint8_t* dst, const float* h) {
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(h[2 * i], h[2 * i + 1]);
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-  d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  store32(dst, o);
 }
 
 // GEMM1 + SwiGLU, round p: thread = accumulator row (token row `prow`);
 // v[0..31] gate and v[32..63] up of intermediate features 64*n_tile + 32p + j.
+// NVFP4: round 0 leaves its 16 code bytes and 2 scale bytes in `carry`, and
+// round 1 stores both rounds' codes (32 bytes) and scales (4 bytes, adjacent
+// in the scale tile) at once.
 template <int FMT>
 __device__ __forceinline__ void epilogue_gemm1(const uint32_t* v, int p, bool store, int64_t prow,
-                                               int n_tile, const GemmArgs& a) {
+                                               int n_tile, const GemmArgs& a,
+                                               uint32_t (&carry)[5]) {
   float h[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i)
@@ -230,22 +240,24 @@ __device__ __forceinline__ void epilogue_gemm1(const uint32_t* v, int p, bool st
     uint8_t sf0, sf1;
     quant_nvfp4_16(h, *reinterpret_cast<uint32_t(*)[2]>(&c[0]), sf0);
     quant_nvfp4_16(h + 16, *reinterpret_cast<uint32_t(*)[2]>(&c[2]), sf1);
-    if (store) {
-      *reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 32 + p * 16) =
-          make_uint4(c[0], c[1], c[2], c[3]);
-      *reinterpret_cast<uint16_t*>(
-          a.out_sf + sf_tile_offset(prow, n_tile * 4 + 2 * p, a.out_sf_tiles_k)) =
-          static_cast<uint16_t>(sf0 | (sf1 << 8));
+    if (p == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) carry[i] = c[i];
+      carry[4] = static_cast<uint32_t>(sf0) | (static_cast<uint32_t>(sf1) << 8);
+    } else if (store) {
+      st_global_v8(a.out + prow * a.out_ld + n_tile * 32, carry[0], carry[1], carry[2], carry[3],
+                   c[0], c[1], c[2], c[3]);
+      st_global_b32_ef(a.out_sf + sf_tile_offset(prow, n_tile * 4, a.out_sf_tiles_k),
+                       carry[4] | (static_cast<uint32_t>(sf0) << 16) |
+                           (static_cast<uint32_t>(sf1) << 24));
     }
   } else if constexpr (FMT == kFmtMXFP8) {
     uint32_t c[8];
     uint8_t sf;
     quant_mxfp8_32(h, c, sf);
     if (store) {
-      uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + p * 32);
-      dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-      dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-      a.out_sf[sf_tile_offset(prow, n_tile * 2 + p, a.out_sf_tiles_k)] = sf;
+      store32(a.out + prow * a.out_ld + n_tile * 64 + p * 32, c);
+      st_global_b8_ef(a.out_sf + sf_tile_offset(prow, n_tile * 2 + p, a.out_sf_tiles_k), sf);
     }
   } else {
     if (store) {
@@ -281,11 +293,8 @@ __device__ __forceinline__ void epilogue_relu2(const uint32_t* v, int p, bool st
       sf4 |= static_cast<uint32_t>(sf) << (8 * jb);
     }
     if (store) {
-      uint4* dst = reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 64 + p * 32);
-      dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-      dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-      *reinterpret_cast<uint32_t*>(
-          a.out_sf + sf_tile_offset(prow, n_tile * 8 + p * 4, a.out_sf_tiles_k)) = sf4;
+      store32(a.out + prow * a.out_ld + n_tile * 64 + p * 32, c);
+      st_global_b32_ef(a.out_sf + sf_tile_offset(prow, n_tile * 8 + p * 4, a.out_sf_tiles_k), sf4);
     }
   } else if constexpr (FMT == kFmtMXFP8) {
 #pragma unroll
@@ -294,11 +303,9 @@ __device__ __forceinline__ void epilogue_relu2(const uint32_t* v, int p, bool st
       uint8_t sf;
       quant_mxfp8_32(h + 32 * jb, c, sf);
       if (store) {
-        uint4* dst =
-            reinterpret_cast<uint4*>(a.out + prow * a.out_ld + n_tile * 128 + p * 64 + jb * 32);
-        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-        a.out_sf[sf_tile_offset(prow, n_tile * 4 + p * 2 + jb, a.out_sf_tiles_k)] = sf;
+        store32(a.out + prow * a.out_ld + n_tile * 128 + p * 64 + jb * 32, c);
+        st_global_b8_ef(a.out_sf + sf_tile_offset(prow, n_tile * 4 + p * 2 + jb, a.out_sf_tiles_k),
+                        sf);
       }
     }
   } else {
@@ -377,9 +384,10 @@ __device__ __forceinline__ void reduce_finish(int64_t t, int n_tile, const GemmA
 
 template <int FMT, int EPI>
 __device__ __forceinline__ void epilogue_round(const uint32_t* v, int p, bool store, int64_t prow,
-                                               int64_t orow, int n_tile, const GemmArgs& a) {
+                                               int64_t orow, int n_tile, const GemmArgs& a,
+                                               uint32_t (&carry)[5]) {
   if constexpr (EPI == 1) {
-    epilogue_gemm1<FMT>(v, p, store, prow, n_tile, a);
+    epilogue_gemm1<FMT>(v, p, store, prow, n_tile, a, carry);
   } else if constexpr (EPI == 3) {
     epilogue_relu2<FMT>(v, p, store, prow, n_tile, a);
   } else if (a.acc) {
@@ -554,7 +562,9 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
     } else if (warp == 2) {
       // ------------------------------------------------ TMA producer
       if (lane == 0) {
-        const uint64_t policy = l2_policy_evict_first();
+        // Decode launches read each weight tile once: evict it first.  Wide
+        // (prefill) launches re-read an expert's tiles for every chunk.
+        const uint64_t policy = NW == 2 ? l2_policy_evict_normal() : l2_policy_evict_first();
         int stage = 0;
         uint32_t phase = 0;
         int slots = 0;          // ring positions used so far
@@ -858,6 +868,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
       const int n128 = it.n_tile * NW + grp;
       if constexpr (NW == 1) {
         if (active) {
+          uint32_t carry[5];
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             uint32_t v[64];
@@ -865,8 +876,8 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
             else epilogue_load<EPI>(taddr, p, v);
             tmem_ld_wait();
             epilogue_fence(v);
-            if (g2) epilogue_round<FMT, 2>(v, p, r < it.rows, prow, orow, n128, A);
-            else epilogue_round<FMT, EPI>(v, p, r < it.rows, prow, orow, n128, A);
+            if (g2) epilogue_round<FMT, 2>(v, p, r < it.rows, prow, orow, n128, A, carry);
+            else epilogue_round<FMT, EPI>(v, p, r < it.rows, prow, orow, n128, A, carry);
           }
         }
         tc_fence_before();
@@ -892,8 +903,9 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
         if (active) {
-          epilogue_round<FMT, EPI>(v, 0, r < it.rows, prow, orow, n128, A);
-          epilogue_round<FMT, EPI>(v + 64, 1, r < it.rows, prow, orow, n128, A);
+          uint32_t carry[5];
+          epilogue_round<FMT, EPI>(v, 0, r < it.rows, prow, orow, n128, A, carry);
+          epilogue_round<FMT, EPI>(v + 64, 1, r < it.rows, prow, orow, n128, A, carry);
         }
       }
     }

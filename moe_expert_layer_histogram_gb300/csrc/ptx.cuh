@@ -118,6 +118,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return pol;
 }
 
+// Weights that several chunks of the same expert read again (prefill).
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
                                                  int32_t x, int32_t y, uint64_t policy) {
   asm volatile(
@@ -309,14 +316,37 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
                : "memory");
 }
 
-// 32-byte global store (one whole L2 sector); the address must be 32-byte
-// aligned.
+// Stores of GEMM outputs that the next kernel reads only after the rest of
+// this one has streamed its operands through L2: marked evict-first, so they
+// do not push out operand tiles that are still being re-read.
+// 32-byte store (one whole L2 sector); the address must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d, uint32_t e, uint32_t f, uint32_t g,
                                              uint32_t h) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a),
-               "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, pol;\n\t}" ::"l"(p),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_global_b32_ef(void* p, uint32_t v) {
+  asm volatile(
+      "{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "st.global.L2::cache_hint.b32 [%0], %1, pol;\n\t}" ::"l"(p),
+      "r"(v)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_global_b8_ef(void* p, uint32_t v) {
+  asm volatile(
+      "{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "st.global.L2::cache_hint.b8 [%0], %1, pol;\n\t}" ::"l"(p),
+      "r"(v)
+      : "memory");
 }
 
 // One 32-bit column of each of the warp's 32 TMEM lanes.
