@@ -131,7 +131,9 @@ moe_status moe_prepare_weights(moe_layer *layer,
 
 /* The layer forward.  hidden: device bf16 [T, H]; router_logits: device f32
  * [T, E]; out: device bf16 [T, H], written in place (never re-bound or
- * reallocated).  0 <= T <= max_tokens; T == 0 is a no-op returning MOE_OK.
+ * reallocated).  hidden and out 16-byte aligned, router_logits 4-byte
+ * aligned (else MOE_ERR_INVALID_ARG).  0 <= T <= max_tokens; T == 0 is a
+ * no-op returning MOE_OK.
  * Asynchronous on `stream`, allocates nothing, never synchronises the host.
  * Results of a later moe_debug_* call describe the latest forward.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_NO_WEIGHTS, MOE_ERR_CUDA (launch).
@@ -146,7 +148,8 @@ moe_status moe_forward(moe_layer *layer, const void *hidden,
  * analysis report, sec. 实现拆解: activations already grouped per expert,
  * a per-expert token count, outputs in the same layout).  hidden: device
  * bf16 [E, M, H]; counts: device int32 [E], rows 0..counts[e]-1 of block e
- * belong to expert e; out: device bf16 [E, M, H].  Each counted row goes
+ * belong to expert e; out: device bf16 [E, M, H]; hidden and out 16-byte
+ * aligned, counts 4-byte aligned.  Each counted row goes
  * through the activation quantisation, GEMM1, the activation with its
  * re-quantisation and GEMM2 of its expert; out receives the bf16 GEMM2
  * output in the same row.  Rows past a count are neither read nor written.
@@ -165,8 +168,10 @@ moe_status moe_forward_batched(moe_layer *layer, const void *hidden,
  * [T,H] bf16 back, all on `stream`; returns once `stream` has finished
  * (synchronises it).  When all three buffers are page-locked host memory
  * the device can address (cudaHostAlloc / cudaHostRegister on a coherent
- * Grace-Blackwell node), the kernels read the inputs and write the output
- * in host memory directly instead of copying.  Errors as moe_forward.    */
+ * Grace-Blackwell node) and aligned as moe_forward asks, the kernels read
+ * the inputs and write the output in host memory directly instead of
+ * copying; host buffers of any alignment go through the copies.  Errors as
+ * moe_forward.                                                            */
 moe_status moe_forward_host(moe_layer *layer, const void *hidden_host,
                             const float *router_logits_host, void *out_host,
                             int T, void *stream);

@@ -427,6 +427,13 @@ moe_status moe_prepare_weights(moe_layer* L, const void* w13, const void* w13_sf
   return MOE_OK;
 }
 
+// The kernels move activations with 16-byte vector accesses and read the
+// logits as fp32.
+bool io_aligned(const void* hidden, const void* logits, const void* out) {
+  return ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(out)) & 15) == 0 &&
+         (reinterpret_cast<uintptr_t>(logits) & 3) == 0;
+}
+
 moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, void* out, int T,
                        void* stream) {
   if (!L || T < 0 || T > L->Tmax) return MOE_ERR_INVALID_ARG;
@@ -435,7 +442,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     L->last_launches = 0;
     return MOE_OK;
   }
-  if (!hidden || !logits || !out) return MOE_ERR_INVALID_ARG;
+  if (!hidden || !logits || !out || !io_aligned(hidden, logits, out)) return MOE_ERR_INVALID_ARG;
   if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int E = L->E, K = L->K, H = L->H;
@@ -500,7 +507,7 @@ moe_status moe_forward_batched(moe_layer* L, const void* hidden, const int32_t* 
                                void* out, void* stream) {
   if (!L || M < 0) return MOE_ERR_INVALID_ARG;
   if (M == 0) return MOE_OK;
-  if (!hidden || !counts || !out) return MOE_ERR_INVALID_ARG;
+  if (!hidden || !counts || !out || !io_aligned(hidden, counts, out)) return MOE_ERR_INVALID_ARG;
   if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
   const int64_t mpad = (static_cast<int64_t>(M) + kRowBlock - 1) / kRowBlock * kRowBlock;
   if (mpad * L->E > L->Rpad) return MOE_ERR_UNSUPPORTED;
@@ -534,7 +541,7 @@ moe_status moe_forward_host(moe_layer* L, const void* hidden_host, const float* 
   void* hd = L->host_zero_copy ? device_view(hidden_host) : nullptr;
   void* ld = L->host_zero_copy ? device_view(logits_host) : nullptr;
   void* od = L->host_zero_copy ? device_view(out_host) : nullptr;
-  if (hd && ld && od) {
+  if (hd && ld && od && io_aligned(hd, ld, od)) {
     moe_status st = moe_forward(L, hd, static_cast<const float*>(ld), od, T, stream);
     if (st != MOE_OK) return st;
     return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -150,6 +150,26 @@ def test_forward_host_matches_device_forward(T, monkeypatch):
     layer.close()
 
 
+def test_forward_host_with_unaligned_pinned_buffers():
+    # pinned but not 16-byte aligned: the host entry point copies instead of
+    # letting the kernels access the buffers in place
+    from moe_expert_layer_histogram_gb300 import moe_forward_host
+    s = workloads.spec("nvfp4_small", T=9)
+    case = workloads.make_case(s, seed=5)
+    stream = torch.cuda.current_stream().cuda_stream
+    layer = make_layer(s, weights=case["weights"])
+    dev_out = run_gpu(layer, case["hidden"], case["logits"]).cpu()
+    n = case["hidden"].numel()
+    hbuf = torch.empty(n + 1, dtype=torch.bfloat16).pin_memory()
+    hbuf[1:] = case["hidden"].reshape(-1)
+    obuf = torch.zeros(n + 1, dtype=torch.bfloat16).pin_memory()
+    lg = case["logits"].contiguous().pin_memory()
+    moe_forward_host(layer.handle, hbuf[1:], lg, obuf[1:], s["T"], stream)
+    assert torch.equal(obuf[1:].view_as(dev_out), dev_out)
+    assert layer.status() == 0
+    layer.close()
+
+
 def test_error_codes():
     from moe_expert_layer_histogram_gb300 import (MoEError, moe_create, moe_destroy,
                                                   moe_forward)
@@ -172,6 +192,13 @@ def test_error_codes():
         moe_forward(h, x, lg, x, 17)                    # T > max_tokens
     assert e.value.code == 1
     moe_forward(h, x, lg, x, 0)                         # T == 0: no-op
+    # the kernels move activations in 16-byte vectors and read fp32 logits:
+    # misaligned buffers are refused before anything is launched
+    for args in ((x.view(-1)[1:], lg, x), (x, lg, x.view(-1)[4:]),
+                 (x, lg.view(torch.uint8).view(-1)[2:], x)):
+        with pytest.raises(MoEError) as e:
+            moe_forward(h, *args, 16)
+        assert e.value.code == 1
     moe_destroy(h)
 
 
@@ -369,6 +396,47 @@ def test_wide_items_match_oracle(name, over, force, monkeypatch):
     assert rel_l2(h, ref["h"]) <= TOL[s["fmt"]], "GEMM2 input"
     assert rel_l2(y, ref["y"]) <= TOL[s["fmt"]], "GEMM2 output"
     assert rel_l2(out.float().cpu().numpy(), bf16_bits_to_f64(ref["out"])) <= TOL[s["fmt"]]
+    layer.close()
+
+
+def test_wide_nvfp4_scale_stagers_and_copies_agree(monkeypatch):
+    # wide NVFP4 GEMM1 items get their scales written into TMEM by four
+    # stager warps (tcgen05.st) or, with MOE_SCALE_STAGER=0, broadcast by the
+    # MMA thread (tcgen05.cp): the same scale values reach the same MMAs, so
+    # the outputs agree bit for bit, and both match the oracle
+    s = workloads.spec("nvfp4_zipf_small", T=1100, E=24, K=4)
+    case = workloads.make_case(s, seed=23)
+    ref = run_oracle(s, case)
+    outs = []
+    for flag in ("1", "0"):
+        monkeypatch.setenv("MOE_SCALE_STAGER", flag)
+        layer = make_layer(s, weights=case["weights"])
+        outs.append(run_gpu(layer, case["hidden"], case["logits"]).cpu())
+        assert layer.status() == 0
+        layer.close()
+    assert torch.equal(outs[0], outs[1])
+    assert rel_l2(outs[0].float().numpy(), bf16_bits_to_f64(ref["out"])) <= TOL["nvfp4"]
+
+
+def test_batched_output_with_16_byte_alignment(monkeypatch):
+    # GEMM2 stores whole 32-byte sectors when the output rows allow it and
+    # 16-byte pieces otherwise: both give the same bytes
+    monkeypatch.setenv("MOE_WIDE_TILES", "1")
+    s = workloads.spec("nvfp4_small", E=3, K=2)
+    M = 40
+    case = workloads.make_case(s, T=1, seed=29)
+    hid, counts = workloads.draw_batched(s, M, seed=29)
+    layer = make_layer(s, max_tokens=s["E"] * 256 // s["K"], weights=case["weights"])
+    ref = layer.forward_batched(hid.cuda(), counts.cuda())
+    buf = torch.zeros(ref.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    off = buf[8:].view_as(ref)                           # 16 bytes past a 256-byte boundary
+    assert off.data_ptr() % 32 == 16
+    layer.forward_batched(hid.cuda(), counts.cuda(), out=off)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    cn = counts.numpy()
+    for e in range(s["E"]):
+        assert torch.equal(off[e, :cn[e]], ref[e, :cn[e]])
     layer.close()
 
 
