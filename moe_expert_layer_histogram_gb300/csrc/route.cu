@@ -53,18 +53,49 @@ __host__ __device__ constexpr int row_units(int H) {
 // Unit `u` of token row x [H] into the padded rows prows[0..n): BF16 copied,
 // MXFP8 / NVFP4 quantised, codes row-major and scales in the MMA's 128-row
 // scale tiles.
+// A unit's bf16 source: 16 (BF16 copy), 32 (NVFP4) or 64 (MXFP8) bytes.
 template <int FMT>
-__device__ __forceinline__ void quant_unit_to_rows(const __nv_bfloat16* __restrict__ x, int H,
-                                                   int u, const int* prows, int n,
-                                                   uint8_t* __restrict__ xq,
-                                                   uint8_t* __restrict__ xsf) {
+struct RawUnit {
+  static constexpr int kVecs = FMT == kFmtBF16 ? 1 : FMT == kFmtNVFP4 ? 2 : 4;
+  uint4 v[kVecs];
+};
+
+template <int FMT>
+__device__ __forceinline__ void load_unit(const __nv_bfloat16* __restrict__ x, int u,
+                                          RawUnit<FMT>& r) {
+  const uint4* src = reinterpret_cast<const uint4*>(x) + static_cast<int64_t>(u) * RawUnit<FMT>::kVecs;
+#pragma unroll
+  for (int i = 0; i < RawUnit<FMT>::kVecs; ++i) r.v[i] = src[i];
+}
+
+template <int N>
+__device__ __forceinline__ void unpack_bf16(const uint4* src, float (&f)[N]) {
+#pragma unroll
+  for (int h = 0; h < N / 8; ++h) {
+    const uint32_t wv[4] = {src[h].x, src[h].y, src[h].z, src[h].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+      f[8 * h + 2 * q] = v.x;
+      f[8 * h + 2 * q + 1] = v.y;
+    }
+  }
+}
+
+// Unit `u` of a token row, already loaded, into the padded rows prows[0..n):
+// BF16 copied, MXFP8 / NVFP4 quantised, codes row-major and scales in the
+// MMA's 128-row scale tiles.
+template <int FMT>
+__device__ __forceinline__ void store_unit_rows(const RawUnit<FMT>& r, int H, int u,
+                                                const int* prows, int n,
+                                                uint8_t* __restrict__ xq,
+                                                uint8_t* __restrict__ xsf) {
   if constexpr (FMT == kFmtBF16) {
-    const uint4 val = reinterpret_cast<const uint4*>(x)[u];
     for (int k = 0; k < n; ++k)
-      reinterpret_cast<uint4*>(xq + static_cast<int64_t>(prows[k]) * H * 2)[u] = val;
+      reinterpret_cast<uint4*>(xq + static_cast<int64_t>(prows[k]) * H * 2)[u] = r.v[0];
   } else if constexpr (FMT == kFmtNVFP4) {
     float f[16];
-    load_bf16<16>(x + u * 16, f);
+    unpack_bf16<16>(r.v, f);
     uint32_t codes[2];
     uint8_t sf;
     quant_nvfp4_16(f, codes, sf);
@@ -75,7 +106,7 @@ __device__ __forceinline__ void quant_unit_to_rows(const __nv_bfloat16* __restri
     }
   } else {
     float f[32];
-    load_bf16<32>(x + u * 32, f);
+    unpack_bf16<32>(r.v, f);
     uint32_t codes[8];
     uint8_t sf;
     quant_mxfp8_32(f, codes, sf);
@@ -89,15 +120,36 @@ __device__ __forceinline__ void quant_unit_to_rows(const __nv_bfloat16* __restri
   }
 }
 
+template <int FMT>
+__device__ __forceinline__ void quant_unit_to_rows(const __nv_bfloat16* __restrict__ x, int H,
+                                                   int u, const int* prows, int n,
+                                                   uint8_t* __restrict__ xq,
+                                                   uint8_t* __restrict__ xsf) {
+  RawUnit<FMT> r;
+  load_unit<FMT>(x, u, r);
+  store_unit_rows<FMT>(r, H, u, prows, n, xq, xsf);
+}
+
 // One warp writes the GEMM1 input of one token row into its padded rows
-// (lane l takes units l, l+32, ...).
+// (lane l takes units l, l+32, ...).  The next unit's load is issued before
+// the current one is quantised and stored, so each lane keeps two loads in
+// flight instead of waiting out the latency of every one.
 template <int FMT>
 __device__ __forceinline__ void quant_row_to_rows(const __nv_bfloat16* __restrict__ x, int H,
                                                   const int* prows, int n,
                                                   uint8_t* __restrict__ xq,
                                                   uint8_t* __restrict__ xsf, int lane) {
-  for (int u = lane; u < row_units<FMT>(H); u += 32)
-    quant_unit_to_rows<FMT>(x, H, u, prows, n, xq, xsf);
+  const int U = row_units<FMT>(H);
+  if (lane >= U) return;
+  RawUnit<FMT> cur;
+  load_unit<FMT>(x, lane, cur);
+  for (int u = lane; u < U; u += 32) {
+    RawUnit<FMT> nxt;
+    const bool more = u + 32 < U;
+    if (more) load_unit<FMT>(x, u + 32, nxt);
+    store_unit_rows<FMT>(cur, H, u, prows, n, xq, xsf);
+    if (more) cur = nxt;
+  }
 }
 
 // ---------------------------------------------------------------- routing
@@ -297,8 +349,8 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
     uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts], cnt[kMaxExperts];
-  __shared__ int s_prow[kTokensPerRouteBlock * kMaxTopK];
+  __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts];
+  __shared__ int s_prow[kTokensPerRouteBlock * kMaxTopK], s_e[kTokensPerRouteBlock * kMaxTopK];
   __shared__ int wsum[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok0 = blockIdx.x * kTokensPerRouteBlock;
@@ -314,12 +366,10 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
   if (e0 < E) {
     s_off[e0] = xo;
     s_poff[e0] = xp;
-    cnt[e0] = 0;
   }
   if (e1 < E) {
     s_off[e1] = xo + c0;
     s_poff[e1] = xp + p0 * kRowBlock;
-    cnt[e1] = 0;
   }
   if (blockIdx.x == 0) {
     if (e0 < E) {
@@ -340,22 +390,24 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
   }
   __syncthreads();
 
-  // 2. stable ranks
-  if (warp == 0) {
-    for (int i = 0; i < ntok; ++i) {
-      const int64_t s = static_cast<int64_t>(tok0 + i) * K + lane;
-      if (lane < K) {
-        const int e = ids[s];
-        const int r = cnt[e] + prefix[static_cast<int64_t>(blockIdx.x) * E + e];
-        cnt[e] += 1;  // the K experts of one token are distinct
-        perm[s_off[e] + r] = static_cast<int32_t>(s);
-        const int prow = s_poff[e] + r;
-        inv[s] = prow;
-        if (prow_slot) prow_slot[prow] = static_cast<int32_t>(s);
-        s_prow[i * K + lane] = prow;
-      }
-      __syncwarp();
-    }
+  // 2. stable ranks, all of the block's slots at once: slot j = i*K + k
+  //    ranks after the block's earlier slots of its expert, which are those
+  //    of earlier tokens (the K experts of one token are distinct), and after
+  //    the earlier blocks' slots (prefix)
+  const int nslot = ntok * K;
+  if (threadIdx.x < nslot) s_e[threadIdx.x] = ids[static_cast<int64_t>(tok0) * K + threadIdx.x];
+  __syncthreads();
+  if (threadIdx.x < nslot) {
+    const int j = threadIdx.x;
+    const int e = s_e[j];
+    int r = prefix[static_cast<int64_t>(blockIdx.x) * E + e];
+    for (int j2 = 0; j2 < j - j % K; ++j2) r += s_e[j2] == e;
+    const int64_t s = static_cast<int64_t>(tok0) * K + j;
+    perm[s_off[e] + r] = static_cast<int32_t>(s);
+    const int prow = s_poff[e] + r;
+    inv[s] = prow;
+    if (prow_slot) prow_slot[prow] = static_cast<int32_t>(s);
+    s_prow[j] = prow;
   }
   __syncthreads();
 
