@@ -20,10 +20,13 @@
 // bytes), B codes (NW x 16 KiB), B scales, A scales.  The MMA always reads
 // 128 A rows; rows past the region only feed accumulator rows that are
 // never stored.  Warp 1 (one thread) owns TMEM: it copies the scale tiles
-// into TMEM (tcgen05.cp; for decode chunks warp 0 writes them with
-// tcgen05.st instead) and issues 128 x (128 NW) tcgen05.mma into an fp32
-// accumulator (two of 128 columns, or one of 256 for wide items).  Warps 3..
-// drain it (tcgen05.ld), run the epilogue and store.  The token tile is the
+// into TMEM (tcgen05.cp) and issues 128 x (128 NW) tcgen05.mma into an fp32
+// accumulator (two of 128 columns, or one of 256 for wide items).  For decode
+// chunks warp 0 writes the scales with tcgen05.st instead, and for wide
+// NVFP4 GEMM1 items four stager warps (12-15, one per TMEM lane quarter) do.
+// The epilogue warps (3.., or 4-11 in the 16-warp wide NVFP4 kernel) drain
+// the accumulator (tcgen05.ld), run the epilogue and store, each thread one
+// row, in whole 32-byte sectors and marked L2 evict-first.  The token tile is the
 // MMA's M (only the chunk's real rows are loaded and stored) and the weight
 // tile its N, so decode-sized chunks cost no extra weight traffic.  Decode
 // launches (T <= 16) run GEMM1 and GEMM2 in one persistent launch (FUSED).
