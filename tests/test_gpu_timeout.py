@@ -2,7 +2,8 @@
 
 The test hook MOE_TEST_STALL_GEMM=1 (read when a layer is created) makes one
 CTA of every GEMM1 launch leave one stage of its shared-memory ring unloaded,
-so the barrier waits on that stage are never satisfied.  Each wait gives up
+so the barrier waits on that stage are never satisfied (in the narrow kernel
+and in the 16-warp wide NVFP4 kernel).  Each wait gives up
 after 2 s: the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its own copies,
 frees its tensor memory and returns.  No fault, trap or hang is involved, and
 the CUDA context stays usable, which the second half checks.
@@ -20,7 +21,12 @@ pytestmark = pytest.mark.gpu
 MOE_ERR_DEVICE_TIMEOUT = 6
 
 
-def test_gemm_wait_runs_out_and_is_reported(monkeypatch):
+@pytest.mark.parametrize("wide", [False, True], ids=["narrow", "wide"])
+def test_gemm_wait_runs_out_and_is_reported(wide, monkeypatch):
+    # wide: the 16-warp NVFP4 kernel, whose scale-stager warps are the ones
+    # waiting on the stage that never lands
+    if wide:
+        monkeypatch.setenv("MOE_WIDE_TILES", "1")
     s = workloads.spec("nvfp4_small")
     case = workloads.make_case(s, seed=21)
     monkeypatch.setenv("MOE_TEST_STALL_GEMM", "1")
