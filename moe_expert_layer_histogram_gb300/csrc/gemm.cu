@@ -526,9 +526,10 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
                 // per 64-element substep j: activation row (lane) scales in
                 // column 8j, the 128 weight rows' scales in columns 8j+4..8j+7
                 uint32_t v[32];
-  #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                  const uint4 b = *reinterpret_cast<const uint4*>(sp + kOffBsf + j * 512 + lane * 16);
+                  const uint4 b =
+                      *reinterpret_cast<const uint4*>(sp + kOffBsf + j * 512 + lane * 16);
                   v[8 * j] = *reinterpret_cast<const uint32_t*>(sp + kOffAsf + j * 512 + lane * 16);
                   v[8 * j + 1] = v[8 * j + 2] = v[8 * j + 3] = 0u;
                   v[8 * j + 4] = b.x;
@@ -622,11 +623,12 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
             } else {
               // codes of both tiles back to back (one 256-row operand), then
               // their scale tiles
-  #pragma unroll
+#pragma unroll
               for (int w = 0; w < NW; ++w) {
                 const uint8_t* src =
                     btile + (static_cast<int64_t>(w) * A.num_kb + kb) * A.b_tile_bytes;
-                bulk_load_hint(sp + A_BYTES + w * kTileBytes, src, kTileBytes, &full[stage], policy);
+                bulk_load_hint(sp + A_BYTES + w * kTileBytes, src, kTileBytes, &full[stage],
+                               policy);
                 if constexpr (SFT > 0)
                   bulk_load_hint(sp + kOffBsf + w * SFT * 512, src + kTileBytes, SFT * 512,
                                  &full[stage], policy);
@@ -694,18 +696,18 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
             if constexpr (FMT == kFmtNVFP4 && NW == 2) {
               if (wstaged) {
                 // the stager warps wrote this stage's scale columns
-  #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 4; ++j)
                   mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
                            sf_col + 32 + j * 4, sf_col + j * 8, (kb | j) != 0);
               } else {
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < 4; ++j) {
                 tc_copy_sf(sf_col + j * 16, desc_sf(smem_u32(sp + kOffAsf + j * 512)));
                 tc_copy_sf(sf_col + j * 16 + 8, desc_sf(smem_u32(sf + j * 512)));
                 tc_copy_sf(sf_col + j * 16 + 12, desc_sf(smem_u32(sf + (SFT + j) * 512)));
               }
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < 4; ++j)
                 mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
                          sf_col + j * 16, sf_col + j * 16 + 8, (kb | j) != 0);
@@ -714,14 +716,14 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
               tc_copy_sf(sf_col, desc_sf(smem_u32(sf)));
               tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf + 512)));
               tc_copy_sf(sf_col + 8, desc_sf(smem_u32(sp + kOffAsf)));
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < 4; ++j)
                 mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
                          idesc_mxf8(128, 256, j), sf_col + 8, sf_col, (kb | j) != 0);
             } else if constexpr (FMT == kFmtNVFP4) {
               if (q0_only && staged) {
                 // lanes 0-31 of the stage's scale columns were written by warp 0
-  #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 4; ++j)
                   mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
                            sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
@@ -732,19 +734,19 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
                 tc_copy_128x256b(sf_col + 8, desc_sf_pair(sfa + 1024, 512));
                 tc_copy_128x256b(sf_col + 16, desc_sf_pair(sfb, 512));
                 tc_copy_128x256b(sf_col + 24, desc_sf_pair(sfb + 1024, 512));
-  #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 4; ++j) {
                   const uint32_t c = (j >> 1) * 8 + (j & 1) * 4;
                   mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
                            sf_col + c, sf_col + 16 + c, (kb | j) != 0);
                 }
               } else {
-  #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 4; ++j) {
                   tc_copy_sf(sf_col + j * 8, desc_sf(smem_u32(sf + (4 + j) * 512)));
                   tc_copy_sf(sf_col + j * 8 + 4, desc_sf(smem_u32(sf + j * 512)));
                 }
-  #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 4; ++j)
                   mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
                            sf_col + j * 8, sf_col + j * 8 + 4, (kb | j) != 0);
@@ -759,12 +761,12 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
                 tc_copy_sf(sf_col, desc_sf(smem_u32(sf)));
                 tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf + 512)));
               }
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < 4; ++j)
                 mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
                          idesc_mxf8(128, 128, j), sf_col + 4, sf_col, (kb | j) != 0);
             } else {
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < 4; ++j)
                 mma_bf16(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
                          (kb | j) != 0);
@@ -805,7 +807,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
             }
             const uint8_t* sp = smem + stage * SB;
             uint32_t v[32];
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint4 b0 = *reinterpret_cast<const uint4*>(sp + kOffBsf + j * 512 + lane * 16);
               const uint4 b1 =
@@ -822,7 +824,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
             const uint32_t col = tmem + (static_cast<uint32_t>(q * 32) << 16) + kSfColBase +
                                  stage * kSfColsPerStage;
             tmem_st32(col, v);
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 4; ++j)
               tmem_st1(col + 32 + 4 * j + q, *reinterpret_cast<const uint32_t*>(
                                                  sp + kOffAsf + j * 512 + lane * 16 + q * 4));

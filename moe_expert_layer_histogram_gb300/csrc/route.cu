@@ -63,7 +63,8 @@ struct RawUnit {
 template <int FMT>
 __device__ __forceinline__ void load_unit(const __nv_bfloat16* __restrict__ x, int u,
                                           RawUnit<FMT>& r) {
-  const uint4* src = reinterpret_cast<const uint4*>(x) + static_cast<int64_t>(u) * RawUnit<FMT>::kVecs;
+  const uint4* src =
+      reinterpret_cast<const uint4*>(x) + static_cast<int64_t>(u) * RawUnit<FMT>::kVecs;
 #pragma unroll
   for (int i = 0; i < RawUnit<FMT>::kVecs; ++i) r.v[i] = src[i];
 }
