@@ -566,9 +566,12 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
     } else if (warp == 2) {
       // ------------------------------------------------ TMA producer
       if (lane == 0) {
-        // Decode launches read each weight tile once: evict it first.  Wide
-        // (prefill) launches re-read an expert's tiles for every chunk.
-        const uint64_t policy = NW == 2 ? l2_policy_evict_normal() : l2_policy_evict_first();
+        // A weight tile is read once per chunk of its expert: experts with a
+        // single chunk (every decode expert) read it once, so it is evicted
+        // first; wide (prefill) launches keep multi-chunk experts' tiles
+        // evict-normal for the later chunks.
+        const uint64_t once = l2_policy_evict_first();
+        const uint64_t reused = NW == 2 ? l2_policy_evict_normal() : once;
         int stage = 0;
         uint32_t phase = 0;
         int slots = 0;          // ring positions used so far
@@ -592,6 +595,8 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
             }
             fence_proxy_async_global();  // generic-proxy stores -> the TMA reads below
           }
+          const uint64_t policy =
+              tab.chunk_off[it.e + 1] - tab.chunk_off[it.e] > 1 ? reused : once;
           const uint32_t bytes = (16u << amap) * 128u + NW * A.b_tile_bytes + SFT * 512u;
           const uint8_t* sfa = A.sfa + static_cast<int64_t>(it.prow0 >> 7) * A.sfa_tiles_k * 512;
           // the item's first 128-row weight tile; the next one (NW = 2)
