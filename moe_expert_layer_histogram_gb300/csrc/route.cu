@@ -131,23 +131,25 @@ __device__ __forceinline__ void quant_unit_to_rows(const __nv_bfloat16* __restri
   store_unit_rows<FMT>(r, H, u, prows, n, xq, xsf);
 }
 
-// One warp writes the GEMM1 input of one token row into its padded rows
-// (lane l takes units l, l+32, ...).  The next unit's load is issued before
-// the current one is quantised and stored, so each lane keeps two loads in
-// flight instead of waiting out the latency of every one.
+// Writes the GEMM1 input of one token row into its padded rows: this thread
+// takes units first, first + stride, ... (one warp: first = lane, stride
+// 32).  The next unit's load is issued before the current one is quantised
+// and stored, so each thread keeps two loads in flight instead of waiting out
+// the latency of every one.
 template <int FMT>
 __device__ __forceinline__ void quant_row_to_rows(const __nv_bfloat16* __restrict__ x, int H,
                                                   const int* prows, int n,
                                                   uint8_t* __restrict__ xq,
-                                                  uint8_t* __restrict__ xsf, int lane) {
+                                                  uint8_t* __restrict__ xsf, int first,
+                                                  int stride = 32) {
   const int U = row_units<FMT>(H);
-  if (lane >= U) return;
+  if (first >= U) return;
   RawUnit<FMT> cur;
-  load_unit<FMT>(x, lane, cur);
-  for (int u = lane; u < U; u += 32) {
+  load_unit<FMT>(x, first, cur);
+  for (int u = first; u < U; u += stride) {
     RawUnit<FMT> nxt;
-    const bool more = u + 32 < U;
-    if (more) load_unit<FMT>(x, u + 32, nxt);
+    const bool more = u + stride < U;
+    if (more) load_unit<FMT>(x, u + stride, nxt);
     store_unit_rows<FMT>(cur, H, u, prows, n, xq, xsf);
     if (more) cur = nxt;
   }
@@ -313,8 +315,8 @@ __global__ void __launch_bounds__(1024) expert_scan_kernel(const int32_t* __rest
     }
 }
 
-// Block-wide exclusive scan of one value per thread (256 threads, each
-// thread's value covering two experts).
+// Block-wide exclusive scan of one value per thread (each thread's value
+// covering two experts; wsum holds one int per warp of the block).
 __device__ __forceinline__ int block_scan_pair(int v, int* wsum) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int inc = v;
@@ -336,13 +338,27 @@ __device__ __forceinline__ int block_scan_pair(int v, int* wsum) {
 //  1. Exclusive scans of the per-expert counts, 128-padded counts and 128-row
 //     chunk counts (every block computes them; block 0 stores them for the
 //     GEMMs).
-//  2. Warp 0 gives each of the block's slots, in slot order, the next row of
-//     its expert after the rows of earlier blocks (stable): perm[row] = slot,
+//  2. Each of the block's slots gets, in slot order, the next row of its
+//     expert after the rows of earlier blocks (stable): perm[row] = slot,
 //     inv[slot] = padded row.
-//  3. Warp w writes token 8b+w's GEMM1 input into its K padded rows: BF16
-//     copied, MXFP8 / NVFP4 quantised per block (one block per lane).
+//  3. W warps per token write token 8b+i's GEMM1 input into its K padded
+//     rows (warp Wi + j takes every W-th 32-unit group from group j): BF16
+//     copied, MXFP8 / NVFP4 quantised per block (one block per thread).
+//     NVFP4 uses W = 2: halving each warp's serial chain of loads and
+//     quantisations took the NVFP4 decode scatter (T = 128, 16 blocks) from
+//     22.8 to 18.8 us.  For the BF16 copy, two warps per row made the bf16
+//     layer 2 us slower, and MXFP8 would lose occupancy (112 registers).
 template <int FMT>
-__global__ void __launch_bounds__(256) scatter_quant_kernel(
+__host__ __device__ constexpr int scatter_warps_per_token() {
+  return FMT == kFmtNVFP4 ? 2 : 1;
+}
+template <int FMT>
+__host__ __device__ constexpr int scatter_threads() {
+  return 32 * kTokensPerRouteBlock * scatter_warps_per_token<FMT>();
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
     const int32_t* __restrict__ ids, int T, int E, int K, const __nv_bfloat16* __restrict__ hidden,
     int H, const int32_t* __restrict__ prefix, const int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ pad_off, int32_t* __restrict__ chunk_off,
@@ -352,7 +368,8 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
   pdl_wait();
   __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts];
   __shared__ int s_prow[kTokensPerRouteBlock * kMaxTopK], s_e[kTokensPerRouteBlock * kMaxTopK];
-  __shared__ int wsum[8];
+  constexpr int W = scatter_warps_per_token<FMT>();
+  __shared__ int wsum[scatter_threads<FMT>() / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok0 = blockIdx.x * kTokensPerRouteBlock;
   const int ntok = min(kTokensPerRouteBlock, T - tok0);
@@ -413,9 +430,10 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
   __syncthreads();
 
   // 3. GEMM1 input rows
-  if (warp >= ntok) return;
-  quant_row_to_rows<FMT>(hidden + static_cast<int64_t>(tok0 + warp) * H, H, s_prow + warp * K, K,
-                         xq, xsf, lane);
+  const int tok = warp / W, part = warp % W;
+  if (tok >= ntok) return;
+  quant_row_to_rows<FMT>(hidden + static_cast<int64_t>(tok0 + tok) * H, H, s_prow + tok * K, K,
+                         xq, xsf, part * 32 + lane, 32 * W);
 }
 
 // ---------------------------------------------------------------- small batches
@@ -718,7 +736,10 @@ cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int 
   auto k = fmt == kFmtBF16 ? scatter_quant_kernel<kFmtBF16>
            : fmt == kFmtMXFP8 ? scatter_quant_kernel<kFmtMXFP8>
                               : scatter_quant_kernel<kFmtNVFP4>;
-  return launch_pdl(g_pdl_small, k, dim3(nb), dim3(256), 0, s, ids, T, E, K, hb, H, prefix,
+  const int threads = fmt == kFmtBF16    ? scatter_threads<kFmtBF16>()
+                      : fmt == kFmtMXFP8 ? scatter_threads<kFmtMXFP8>()
+                                         : scatter_threads<kFmtNVFP4>();
+  return launch_pdl(g_pdl_small, k, dim3(nb), dim3(threads), 0, s, ids, T, E, K, hb, H, prefix,
                     counts, offsets, pad_off, chunk_off, perm, inv, prow_slot, xq, xsf);
 }
 
