@@ -26,23 +26,6 @@ namespace {
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // ---------------------------------------------------------------- row quantisation
-// bf16 -> fp32 for N consecutive elements (N a multiple of 8, 16-byte aligned).
-template <int N>
-__device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float (&f)[N]) {
-  const uint4* src = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-  for (int h = 0; h < N / 8; ++h) {
-    const uint4 u = src[h];
-    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
-      f[8 * h + 2 * q] = v.x;
-      f[8 * h + 2 * q + 1] = v.y;
-    }
-  }
-}
-
 // Units of one token row's GEMM1 input: 16-byte chunks (BF16, copied) or
 // quantisation blocks of 16 (NVFP4) / 32 (MXFP8) elements.
 template <int FMT>
