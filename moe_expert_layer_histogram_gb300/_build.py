@@ -2,7 +2,7 @@
 
 sm_103a only (GB300).  The translation units compile in parallel; the host
 runtime links the CUDA runtime statically, so the library needs nothing but
-the driver at load time.
+the CUDA driver (libcuda) at load time.
 """
 import concurrent.futures as cf
 import os
