@@ -95,6 +95,17 @@ typedef struct {
                           with MOE_ACT_RELU2 is MOE_ERR_UNSUPPORTED)        */
     int activation;    /* moe_activation (0 = SwiGLU)                       */
     int combine;       /* moe_combine (0 = gather)                          */
+    int max_ctas;      /* > 0: at most this many CTAs per GEMM launch (to
+                          share the GPU with concurrent work); 0: one CTA
+                          per SM                                            */
+    /* Fault injection for the library's own tests; 0 = off.  Nothing else
+     * turns these on (they are not read from the environment).            */
+    int test_fail_alloc_at; /* n > 0: the n-th device allocation made by
+                               moe_create fails (MOE_ERR_OOM, nothing leaks) */
+    int test_stall_gemm;    /* 1: CTA 0 of every GEMM1 launch leaves one
+                               shared-memory stage unloaded, so the waits on
+                               it run out after 2 s and the forward records
+                               MOE_ERR_DEVICE_TIMEOUT (no fault, no hang)   */
 } moe_config;
 
 typedef struct moe_layer moe_layer;   /* opaque */
@@ -102,13 +113,21 @@ typedef struct moe_layer moe_layer;   /* opaque */
 /* Create a layer on the current CUDA device.  Validates `cfg` and allocates
  * every device buffer a forward of up to cfg->max_tokens tokens needs
  * (weights, routing tables, permuted activations, intermediates), so that
- * moe_forward never allocates.  *out receives the handle (NULL on error).
+ * moe_forward never allocates: the workspace is sized once by the largest
+ * token count, as MegaMoE sizes its own by num_max_tokens (MegaMoE
+ * kernel-drop workflow page, sec. 六).  E and K are fixed here and every
+ * launch uses this E (a global-vs-local expert count mismatch broke the
+ * b12x integration: PR #40082 report, sec. 风险与影响 item 3).  *out receives the handle (NULL on error).
  * Errors: MOE_ERR_INVALID_ARG (NULL args), MOE_ERR_UNSUPPORTED (shape),
  * MOE_ERR_NO_DEVICE, MOE_ERR_OOM (nothing leaks), MOE_ERR_CUDA.            */
 moe_status moe_create(const moe_config *cfg, moe_layer **out);
 
 /* Copy the canonical weights into the layer's own buffers and transform them
- * into the kernels' layout (untimed set-up, enqueued on `stream`; returns
+ * into the kernels' layout once, at load time rather than per forward, with
+ * the NVFP4 global scale folded into the block scales (the b12x
+ * process_weights_after_loading step: PR #40082 report, sec. 关键源码片段;
+ * the scale-layout conversion moved to load time: same report, sec.
+ * 评论区精华) (untimed set-up, enqueued on `stream`; returns
  * after enqueueing, the caller may free its buffers once `stream` has
  * finished).  All pointers are device pointers, row-major, reduction
  * dimension contiguous; W13 rows 0..I-1 are the gate projection and rows
@@ -129,9 +148,13 @@ moe_status moe_prepare_weights(moe_layer *layer,
                                const void *w2, const void *w2_sf,
                                const float *w2_gs, void *stream);
 
-/* The layer forward.  hidden: device bf16 [T, H]; router_logits: device f32
- * [T, E]; out: device bf16 [T, H], written in place (never re-bound or
- * reallocated).  hidden and out 16-byte aligned, router_logits 4-byte
+/* The layer forward: routing, permutation, activation quantisation, GEMM1,
+ * SwiGLU, GEMM2 and the combine on bf16 hidden states, as the b12x call runs
+ * them (PR #40082 report, sec. 实现拆解 item 1).  hidden: device bf16 [T, H];
+ * router_logits: device f32 [T, E]; out: device bf16 [T, H], written in
+ * place, never re-bound or reallocated (a backend that re-bound its output
+ * left the caller's buffer unwritten: PR 38050 analysis report, sec.
+ * 评论区精华).  hidden and out 16-byte aligned, router_logits 4-byte
  * aligned (else MOE_ERR_INVALID_ARG).  0 <= T <= max_tokens; T == 0 is a
  * no-op returning MOE_OK.
  * Asynchronous on `stream`, allocates nothing, never synchronises the host.
@@ -163,7 +186,8 @@ moe_status moe_forward_batched(moe_layer *layer, const void *hidden,
                                const int32_t *counts, int M, void *out,
                                void *stream);
 
-/* Same as moe_forward with HOST buffers: copies hidden [T,H] bf16 and
+/* (The build's own call, for the end-to-end measurement.)  Same as
+ * moe_forward with HOST buffers: copies hidden [T,H] bf16 and
  * router_logits [T,E] f32 to the device, runs the layer and copies out
  * [T,H] bf16 back, all on `stream`; returns once `stream` has finished
  * (synchronises it).  When all three buffers are page-locked host memory
@@ -176,34 +200,55 @@ moe_status moe_forward_host(moe_layer *layer, const void *hidden_host,
                             const float *router_logits_host, void *out_host,
                             int T, void *stream);
 
-/* Inspection of the latest forward (tests): device destinations, any may be
- * NULL.  topk_ids int32 [T,K], topk_w f32 [T,K], offsets int32 [E+1]
+/* Inspection of the latest forward (tests; the build's own call, no
+ * counterpart on the pages): device destinations, any may be NULL.  topk_ids int32 [T,K], topk_w f32 [T,K], offsets int32 [E+1]
  * (offsets[e] = first permuted row of expert e, offsets[E] = T*K),
  * perm int32 [T*K] (permuted row -> slot t*K+k).  Enqueued on `stream`.   */
 moe_status moe_debug_routing(moe_layer *layer, int32_t *topk_ids,
                              float *topk_w, int32_t *offsets, int32_t *perm,
                              void *stream);
 
-/* GEMM1 input quantisation of the latest forward, per token, canonical
- * layout: codes [T, H/2] (NVFP4) or [T, H] (MXFP8), scales [T, H/16] or
+/* GEMM1 input quantisation of the latest forward (tests; the build's own
+ * call), per token, canonical layout: codes [T, H/2] (NVFP4) or [T, H] (MXFP8), scales [T, H/16] or
  * [T, H/32].  Device destinations.  MOE_ERR_UNSUPPORTED for BF16.         */
 moe_status moe_debug_act_quant(moe_layer *layer, uint8_t *codes,
                                uint8_t *scales, void *stream);
 
-/* GEMM2 input (SwiGLU output after re-quantisation, dequantised to f32,
+/* (Tests; the build's own call.)  GEMM2 input (SwiGLU output after
+ * re-quantisation, dequantised to f32,
  * [T*K, I]) and GEMM2 output (f32 of the stored bf16, [T*K, H]) of the
  * latest forward, in permuted row order.  Device destinations, may be NULL. */
 moe_status moe_debug_intermediates(moe_layer *layer, float *h, float *y,
                                    void *stream);
 
-/* Device-side error word of the handle: synchronises the device, returns
+/* The prepared weight tiles of one expert, as moe_prepare_weights left them
+ * (inspection for tests of the weight preparation).  which = 13 (W13) or
+ * 2 (W2); dst: device or host destination of exactly dst_bytes =
+ * (N/128) * (K_bytes/128) * tile_bytes, where N is the matrix's rows (W13:
+ * 2I, or I for ReLU^2; W2: H), K_bytes its row length in bytes (H or I
+ * times 2, 1 or 1/2 for BF16 / MXFP8 / NVFP4) and tile_bytes 16384 plus
+ * 512 per scale tile (NVFP4 4, MXFP8 1, BF16 0).  Layout: tiles ordered by
+ * 128-row block, then 128-byte K slice; a tile is 128 rows x 128 bytes of
+ * codes, 16-byte chunk c of row r at byte r*128 + (c ^ (r % 8))*16 (the
+ * 128-byte swizzle), then the slice's scale tiles, scale j of tile row r at
+ * (r % 32)*16 + (r / 32)*4 + j.  W13 rows are interleaved in groups of
+ * 64 for SwiGLU: prepared row 128g + r is gate row 64g + r for r < 64 and
+ * up row I + 64g + r - 64 otherwise.  NVFP4 scales are the folded ones
+ * (e4m3(float(sf) * gs)).  Errors: MOE_ERR_INVALID_ARG (bad which, expert
+ * or size), MOE_ERR_NO_WEIGHTS, MOE_ERR_CUDA.  Enqueued on `stream`.
+ * The build's own inspection call; the pages have no counterpart.        */
+moe_status moe_debug_weight_tiles(moe_layer *layer, int which, int expert,
+                                  void *dst, size_t dst_bytes, void *stream);
+
+/* Device-side error word of the handle (the build's own call; the pages
+ * have no counterpart): synchronises the device, returns
  * the first error a kernel recorded since the last call (and clears it):
  * MOE_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait,
  * MOE_ERR_INVALID_ARG if moe_forward_batched met a count outside [0, M];
  * MOE_ERR_CUDA on a sticky CUDA error; else MOE_OK.                        */
 moe_status moe_get_status(moe_layer *layer);
 
-/* Per-kernel timing (profiling).  While on, every moe_forward records a CUDA
+/* Per-kernel timing (profiling; the build's own call).  While on, every moe_forward records a CUDA
  * event before each of its six kernels and one after the last, for at most
  * max_forwards forwards; the events are created here, not in the forward.
  * moe_timing_stop waits for the recorded work, writes the summed duration
@@ -216,7 +261,8 @@ moe_status moe_get_status(moe_layer *layer);
 moe_status moe_timing_start(moe_layer *layer, int max_forwards);
 moe_status moe_timing_stop(moe_layer *layer, float *kernel_ms, int *forwards);
 
-/* Number of kernel launches the latest moe_forward enqueued.              */
+/* Number of kernel launches the latest moe_forward enqueued (the build's
+ * own call).                                                              */
 int moe_last_launch_count(const moe_layer *layer);
 
 /* Routing and expert permutation without any device allocation.  The pages
@@ -234,8 +280,10 @@ int moe_last_launch_count(const moe_layer *layer);
  * up that array's device address (make that first call before any stream
  * capture).  All calls share the array: calls whose work overlaps on the
  * GPU (other streams, unordered host threads) race and give wrong results.
- * Errors: MOE_ERR_INVALID_ARG (T < 0, K > E, NULL pointer),
- * MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.  T == 0 is a no-op.                  */
+ * Errors: MOE_ERR_INVALID_ARG (T < 0, K > E, a NULL or not 4-byte aligned
+ * pointer; found on the host, nothing is launched), MOE_ERR_UNSUPPORTED,
+ * MOE_ERR_CUDA (a launch failed; earlier errors of the context are neither
+ * reported nor cleared).  T == 0 is a no-op.                               */
 moe_status moe_route_permute_static(const float *router_logits, int T, int E,
                                     int K, int32_t *topk_ids, float *topk_w,
                                     int32_t *offsets, int32_t *perm,
@@ -257,11 +305,12 @@ moe_status moe_route_permute_static(const float *router_logits, int T, int E,
 moe_status moe_measure_mma_rate(int format, int n_cols, int copy_scales,
                                 int iters, double *tflops, void *stream);
 
-/* Static description of a status code (never NULL).                       */
+/* Static description of a status code (never NULL; the build's own call). */
 const char *moe_status_string(moe_status s);
 
 /* Free everything the handle owns.  NULL-safe.  Synchronises the device
- * first so no enqueued work still uses the buffers.                        */
+ * first so no enqueued work still uses the buffers.  (The build's own call:
+ * the pages manage the layer's memory through the framework.)            */
 void moe_destroy(moe_layer *layer);
 
 #ifdef __cplusplus

@@ -29,7 +29,8 @@ class MoEConfig(ctypes.Structure):
                 ("inter", ctypes.c_int), ("num_experts", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("format", ctypes.c_int),
                 ("clamp_limit", ctypes.c_float), ("activation", ctypes.c_int),
-                ("combine", ctypes.c_int)]
+                ("combine", ctypes.c_int), ("max_ctas", ctypes.c_int),
+                ("test_fail_alloc_at", ctypes.c_int), ("test_stall_gemm", ctypes.c_int)]
 
 
 class MoEError(RuntimeError):
@@ -42,6 +43,7 @@ class MoEError(RuntimeError):
 EXPORTS = ("moe_create", "moe_prepare_weights", "moe_forward", "moe_forward_batched",
            "moe_forward_host",
            "moe_debug_routing", "moe_debug_act_quant", "moe_debug_intermediates",
+           "moe_debug_weight_tiles",
            "moe_get_status", "moe_timing_start", "moe_timing_stop", "moe_last_launch_count",
            "moe_route_permute_static", "moe_measure_mma_rate", "moe_status_string",
            "moe_destroy")
@@ -66,6 +68,7 @@ def lib():
     L.moe_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp]
     L.moe_debug_act_quant.argtypes = [vp, vp, vp, vp]
     L.moe_debug_intermediates.argtypes = [vp, vp, vp, vp]
+    L.moe_debug_weight_tiles.argtypes = [vp, ci, ci, vp, ctypes.c_size_t, vp]
     L.moe_get_status.argtypes = [vp]
     L.moe_timing_start.argtypes = [vp, ci]
     L.moe_timing_stop.argtypes = [vp, vp, vp]
@@ -102,11 +105,13 @@ def moe_status_string(code):
 
 
 def moe_create(max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit=0.0,
-               activation="swiglu", combine="gather"):
+               activation="swiglu", combine="gather", max_ctas=0, test_fail_alloc_at=0,
+               test_stall_gemm=0):
     cfg = MoEConfig(int(max_tokens), int(hidden), int(inter), int(num_experts), int(top_k),
                     MOE_FMT[fmt] if isinstance(fmt, str) else int(fmt), float(clamp_limit or 0.0),
                     MOE_ACT[activation] if isinstance(activation, str) else int(activation),
-                    MOE_COMBINE[combine] if isinstance(combine, str) else int(combine))
+                    MOE_COMBINE[combine] if isinstance(combine, str) else int(combine),
+                    int(max_ctas), int(test_fail_alloc_at), int(test_stall_gemm))
     h = ctypes.c_void_p()
     _check(lib().moe_create(ctypes.byref(cfg), ctypes.byref(h)), "moe_create")
     return h.value
@@ -146,6 +151,14 @@ def moe_debug_act_quant(handle, codes, scales, stream=None):
 def moe_debug_intermediates(handle, h=None, y=None, stream=None):
     _check(lib().moe_debug_intermediates(handle, _ptr(h), _ptr(y), stream),
            "moe_debug_intermediates")
+
+
+def moe_debug_weight_tiles(handle, which, expert, dst, stream=None):
+    """Copy expert `expert`'s prepared W13 (which=13) or W2 (which=2) tiles
+    into `dst` (a uint8 tensor of exactly the tiles' size)."""
+    _check(lib().moe_debug_weight_tiles(handle, int(which), int(expert), _ptr(dst),
+                                        dst.numel() * dst.element_size(), stream),
+           "moe_debug_weight_tiles")
 
 
 def moe_get_status(handle):
@@ -202,14 +215,14 @@ class MoELayer:
     work goes on torch's current stream."""
 
     def __init__(self, max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit=0.0,
-                 activation="swiglu", combine="gather"):
+                 activation="swiglu", combine="gather", **config):
         import torch
         self.torch = torch
         self.H, self.I, self.E, self.K = hidden, inter, num_experts, top_k
         self.fmt = fmt
         self.max_tokens = max_tokens
         self.handle = moe_create(max_tokens, hidden, inter, num_experts, top_k, fmt, clamp_limit,
-                                 activation, combine)
+                                 activation, combine, **config)
         self.T = 0
 
     def _stream(self):

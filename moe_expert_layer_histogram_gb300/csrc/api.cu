@@ -57,7 +57,8 @@ struct moe_layer {
   int pair_scale_copies = 1;
   int wide_tiles = -1;               // 0 off, 1 always, -1 for prefill-sized launches
   int stage_scales = 1;              // decode scales written by a warp, not copied
-  int test_stall = 0;                // test hook (MOE_TEST_STALL_GEMM): GEMM1 times out
+  int test_stall = 0;                // fault injection (moe_config.test_stall_gemm): GEMM1 times out
+  int max_ctas = 0;                  // CTAs per GEMM launch (moe_config.max_ctas, else the SM count)
   bool weights_ready = false;
   int last_T = 0, last_launches = 0;
   std::vector<cudaEvent_t> tev;  // per-kernel timing events, 7 per forward
@@ -93,16 +94,13 @@ bool make_map(CUtensorMap* m, void* base, uint64_t row_bytes, uint64_t rows, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Test hook: MOE_TEST_FAIL_ALLOC_AT=n makes the n-th device allocation of
-// moe_create fail, so tests can check that the error is reported and nothing
-// leaks, without exhausting the GPU.
+// Device allocations of moe_create.  moe_config.test_fail_alloc_at = n makes
+// the n-th one fail, so tests can check that the error is reported and
+// nothing leaks, without exhausting the GPU.
 struct Allocator {
   moe_layer* L;
   int count = 0, fail_at = 0;
-  explicit Allocator(moe_layer* l) : L(l) {
-    const char* v = std::getenv("MOE_TEST_FAIL_ALLOC_AT");
-    fail_at = v ? std::atoi(v) : 0;
-  }
+  Allocator(moe_layer* l, int fail) : L(l), fail_at(fail) {}
   template <class T>
   bool get(T** p, size_t bytes) {
     ++count;
@@ -210,7 +208,7 @@ cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
                       cudaStream_t s) {
   wide = wide && L->w13_rows % 256 == 0;
   const GemmArgs a = gemm1_args(L, pair, wide);
-  const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
+  const int grid = static_cast<int>(std::min<int64_t>(L->max_ctas, chunks * a.n_tiles));
   return launch_gemm(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a, grid, max_rows, wide,
                      s);
 }
@@ -219,7 +217,7 @@ cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool
                       int rows_per_expert, cudaStream_t s, void* reduce_out = nullptr) {
   wide = wide && L->H % 256 == 0;
   const GemmArgs a = gemm2_args(L, pair, wide, out, rows_per_expert, reduce_out);
-  const int grid = static_cast<int>(std::min<int64_t>(L->num_sms, chunks * a.n_tiles));
+  const int grid = static_cast<int>(std::min<int64_t>(L->max_ctas, chunks * a.n_tiles));
   return launch_gemm(L->fmt, 2, L->maps2, a, grid, max_rows, wide, s);
 }
 
@@ -232,7 +230,7 @@ cudaError_t run_gemms_fused(moe_layer* L, int64_t chunks, int max_rows, int pair
   a1.done1 = L->done1;
   const GemmArgs a2 = gemm2_args(L, pair, false, L->y, 0, reduce_out);
   const int grid = static_cast<int>(
-      std::min<int64_t>(L->num_sms, chunks * (a1.n_tiles + a2.n_tiles)));
+      std::min<int64_t>(L->max_ctas, chunks * (a1.n_tiles + a2.n_tiles)));
   return launch_gemm_fused(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a1, L->maps2, a2,
                            grid, max_rows, s);
 }
@@ -276,6 +274,8 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   if (c.format < MOE_FMT_BF16 || c.format > MOE_FMT_NVFP4) return MOE_ERR_INVALID_ARG;
   if (c.activation != MOE_ACT_SWIGLU && c.activation != MOE_ACT_RELU2) return MOE_ERR_INVALID_ARG;
   if (c.combine != MOE_COMBINE_GATHER && c.combine != MOE_COMBINE_REDUCE) return MOE_ERR_INVALID_ARG;
+  if (c.max_ctas < 0 || c.test_fail_alloc_at < 0 || c.test_stall_gemm < 0 || c.test_stall_gemm > 1)
+    return MOE_ERR_INVALID_ARG;
   if (c.activation == MOE_ACT_RELU2 && c.clamp_limit > 0.0f && std::isfinite(c.clamp_limit))
     return MOE_ERR_UNSUPPORTED;
   const int kq = c.format == MOE_FMT_NVFP4 ? 256 : 128;
@@ -336,10 +336,11 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   // MOE_SCALE_STAGER=0: decode chunks copy their scales with tcgen05.cp
   // (lanes 0-31 through 128x256b copies) instead of a staging warp.
   if (const char* sv = std::getenv("MOE_SCALE_STAGER")) L->stage_scales = sv[0] != '0';
-  // Test hook for the bounded waits: MOE_TEST_STALL_GEMM=1 makes one CTA of
-  // every GEMM1 launch leave one stage unloaded; its waits give up after
-  // 2 s and moe_get_status reports MOE_ERR_DEVICE_TIMEOUT.
-  if (const char* tv = std::getenv("MOE_TEST_STALL_GEMM")) L->test_stall = tv[0] == '1';
+  // Fault injection for the bounded waits (tests only, through the config):
+  // one CTA of every GEMM1 launch leaves one stage unloaded; its waits give
+  // up after 2 s and moe_get_status reports MOE_ERR_DEVICE_TIMEOUT.
+  L->test_stall = c.test_stall_gemm == 1;
+  L->max_ctas = c.max_ctas > 0 ? std::min(c.max_ctas, sms) : sms;
   // MOE_FUSED_GEMMS=0: decode launches keep GEMM1 and GEMM2 separate.
   if (const char* fv = std::getenv("MOE_FUSED_GEMMS")) L->fused_gemms = fv[0] != '0';
   // MOE_HOST_ZERO_COPY=0: moe_forward_host always copies through device buffers.
@@ -353,7 +354,7 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
     L->xb = 2 * H; L->hb = 2 * I; L->x_tiles_k = 0; L->h_tiles_k = 0;
   }
   const size_t rblocks = static_cast<size_t>(Rpad / kRowBlock);
-  Allocator A(L);
+  Allocator A(L, c.test_fail_alloc_at);
   bool ok = A.get(&L->ids, Rmax * 4) && A.get(&L->w, Rmax * 4) &&
             A.get(&L->blockhist, static_cast<size_t>(L->NBmax) * E * 4) &&
             A.get(&L->prefix, static_cast<size_t>(L->NBmax) * E * 4) &&
@@ -578,6 +579,23 @@ moe_status moe_debug_act_quant(moe_layer* L, uint8_t* codes, uint8_t* scales, vo
   if (L->last_T == 0) return MOE_OK;
   return launch_debug_act(L->fmt, L->inv, L->last_T, L->K, L->H, L->xq, L->xsf, codes, scales,
                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+moe_status moe_debug_weight_tiles(moe_layer* L, int which, int expert, void* dst,
+                                  size_t dst_bytes, void* stream) {
+  if (!L || !dst || (which != 13 && which != 2) || expert < 0 || expert >= L->E)
+    return MOE_ERR_INVALID_ARG;
+  if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
+  const int rows = which == 13 ? L->w13_rows : L->H;
+  const int row_bytes = which == 13 ? L->xb : L->hb;
+  const size_t per_expert =
+      static_cast<size_t>(rows / 128) * (row_bytes / 128) * weight_tile_bytes(L->fmt);
+  if (dst_bytes != per_expert) return MOE_ERR_INVALID_ARG;
+  const uint8_t* src = (which == 13 ? L->w13t : L->w2t) + per_expert * expert;
+  return cudaMemcpyAsync(dst, src, per_expert, cudaMemcpyDefault,
+                         static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }

@@ -18,6 +18,7 @@
 
 #include "internal.h"
 #include "quant.cuh"
+#include "route_token.cuh"
 
 namespace moe {
 
@@ -139,64 +140,8 @@ __device__ __forceinline__ void quant_row_to_rows(const __nv_bfloat16* __restric
 }
 
 // ---------------------------------------------------------------- routing
-// One warp per token, 8 tokens per block.  Lane l holds logits l, l+32, ...;
-// K rounds of a warp arg-max in the total order (value descending, index
-// ascending), then the softmax of the K selected values.  Block b also counts
+// One warp per token (route_token), 8 tokens per block.  Block b also counts
 // how many of its slots go to each expert (blockhist[b][e]).
-// One warp routes the token with logits l[E]: lane k < K receives the k-th
-// expert in *id and its softmax weight in *wt.
-template <int MAXJ>
-__device__ __forceinline__ void route_token(const float* __restrict__ l, int E, int K, int lane,
-                                            int* id, float* wt) {
-  float my_v = 0.0f;
-  int my_i = 0;
-  {
-    float v[MAXJ];
-    uint32_t avail = 0;
-#pragma unroll
-    for (int j = 0; j < MAXJ; ++j) {
-      const int e = lane + 32 * j;
-      v[j] = -FLT_MAX;
-      if (e < E) {
-        v[j] = __ldg(l + e);
-        avail |= 1u << j;
-      }
-    }
-    for (int k = 0; k < K; ++k) {
-      float bv = -FLT_MAX;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int j = 0; j < MAXJ; ++j)
-        if (((avail >> j) & 1u) && (bi == INT_MAX || v[j] > bv)) {
-          bv = v[j];
-          bi = lane + 32 * j;
-        }
-#pragma unroll
-      for (int off = 16; off; off >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, off);
-        const int oi = __shfl_xor_sync(kFull, bi, off);
-        const bool take = oi != INT_MAX && (bi == INT_MAX || ov > bv || (ov == bv && oi < bi));
-        if (take) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
-      if (lane == k) {
-        my_v = bv;
-        my_i = bi;
-      }
-    }
-  }
-  const float m = __shfl_sync(kFull, my_v, 0);
-  const float ex = lane < K ? expf(my_v - m) : 0.0f;
-  float sum = ex;
-#pragma unroll
-  for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-  *id = my_i;
-  *wt = ex / sum;
-}
-
 template <int MAXJ>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E,
                                                     int K, int32_t* __restrict__ ids,

@@ -21,12 +21,11 @@
 // has to be cleared between calls; but two calls whose kernels overlap on the
 // GPU (different streams, or different host threads without ordering) race
 // on the array and produce garbage.
-#include <cfloat>
-#include <climits>
 #include <mutex>
 
 #include "internal.h"
 #include "moe.h"
+#include "route_token.cuh"
 
 namespace moe {
 
@@ -42,8 +41,8 @@ static __device__ __align__(256) int32_t g_static_scratch[kStaticScratchInts];
 
 constexpr unsigned kAll = 0xFFFFFFFFu;
 
-// One warp per token: top-K (value descending, index ascending) and softmax
-// over the K selected logits; block b counts its 64 tokens' slots per expert.
+// One warp per token (route_token, the same router moe_forward uses); block
+// b counts its 64 tokens' slots per expert.
 __global__ void __launch_bounds__(256) static_route_kernel(const float* __restrict__ logits, int T,
                                                            int E, int K, int32_t* __restrict__ ids,
                                                            float* __restrict__ w,
@@ -55,52 +54,12 @@ __global__ void __launch_bounds__(256) static_route_kernel(const float* __restri
   for (int i = warp; i < kStaticBlockTokens; i += 8) {
     const int t = blockIdx.x * kStaticBlockTokens + i;
     if (t >= T) break;
-    const float* l = logits + static_cast<int64_t>(t) * E;
-    float v[16];
-    uint32_t avail = 0;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int e = lane + 32 * j;
-      v[j] = -FLT_MAX;
-      if (e < E) {
-        v[j] = l[e];
-        avail |= 1u << j;
-      }
-    }
-    float my_v = 0.0f;
-    int my_i = 0;
-    for (int k = 0; k < K; ++k) {
-      float bv = -FLT_MAX;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (((avail >> j) & 1u) && (bi == INT_MAX || v[j] > bv)) {
-          bv = v[j];
-          bi = lane + 32 * j;
-        }
-#pragma unroll
-      for (int off = 16; off; off >>= 1) {
-        const float ov = __shfl_xor_sync(kAll, bv, off);
-        const int oi = __shfl_xor_sync(kAll, bi, off);
-        if (oi != INT_MAX && (bi == INT_MAX || ov > bv || (ov == bv && oi < bi))) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
-      if (lane == k) {
-        my_v = bv;
-        my_i = bi;
-      }
-    }
-    const float m = __shfl_sync(kAll, my_v, 0);
-    const float ex = lane < K ? expf(my_v - m) : 0.0f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(kAll, sum, off);
+    int my_i;
+    float my_w;
+    route_token<kMaxExperts / 32>(logits + static_cast<int64_t>(t) * E, E, K, lane, &my_i, &my_w);
     if (lane < K) {
       ids[static_cast<int64_t>(t) * K + lane] = my_i;
-      w[static_cast<int64_t>(t) * K + lane] = ex / sum;
+      w[static_cast<int64_t>(t) * K + lane] = my_w;
       atomicAdd(&hist[my_i], 1);
     }
   }
@@ -189,6 +148,9 @@ cudaError_t static_scratch(int32_t** out) {
 
 }  // namespace moe
 
+// Every pointer is read or written as 32-bit words by the kernels.
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+
 extern "C" moe_status moe_route_permute_static(const float* router_logits, int T, int E, int K,
                                                int32_t* topk_ids, float* topk_w,
                                                int32_t* offsets, int32_t* perm, void* stream) {
@@ -197,17 +159,27 @@ extern "C" moe_status moe_route_permute_static(const float* router_logits, int T
   if (T > kStaticMaxTokens || E > kMaxExperts || K > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!router_logits || !topk_ids || !topk_w || !offsets || !perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned4(router_logits) || !aligned4(topk_ids) || !aligned4(topk_w) ||
+      !aligned4(offsets) || !aligned4(perm))
+    return MOE_ERR_INVALID_ARG;
   int32_t* scratch = nullptr;
   if (static_scratch(&scratch) != cudaSuccess) {
-    cudaGetLastError();
+    cudaGetLastError();  // the failed look-up's own error, not a sticky one
     return MOE_ERR_CUDA;
   }
   int32_t* hist = scratch;
   int32_t* base = scratch + kStaticMaxBlocks * kMaxExperts;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int NB = (T + kStaticBlockTokens - 1) / kStaticBlockTokens;
-  static_route_kernel<<<NB, 256, 0, s>>>(router_logits, T, E, K, topk_ids, topk_w, hist);
-  static_scan_kernel<<<1, kMaxExperts, 0, s>>>(hist, NB, E, offsets, base);
-  static_rank_kernel<<<NB, 32, 0, s>>>(topk_ids, T, E, K, base, perm);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  // each launch reports its own error; an earlier, unrelated error of the
+  // context is neither reported here nor cleared
+  cudaError_t e = launch_pdl(false, static_route_kernel, dim3(NB), dim3(256), 0, s, router_logits,
+                             T, E, K, topk_ids, topk_w, hist);
+  if (e == cudaSuccess)
+    e = launch_pdl(false, static_scan_kernel, dim3(1), dim3(kMaxExperts), 0, s, hist, NB, E,
+                   offsets, base);
+  if (e == cudaSuccess)
+    e = launch_pdl(false, static_rank_kernel, dim3(NB), dim3(32), 0, s, topk_ids, T, E, K, base,
+                   perm);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -24,11 +24,12 @@ def bf16_bits_to_f64(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def make_layer(s, max_tokens=None, weights=None, device="cuda:0"):
+def make_layer(s, max_tokens=None, weights=None, device="cuda:0", **config):
+    """config: further moe_config fields (max_ctas, test_stall_gemm, ...)."""
     import torch
     from moe_expert_layer_histogram_gb300 import MoELayer
     layer = MoELayer(max_tokens or s["T"], s["H"], s["I"], s["E"], s["K"], s["fmt"], s["clamp"],
-                     s.get("act", "swiglu"), s.get("combine", "gather"))
+                     s.get("act", "swiglu"), s.get("combine", "gather"), **config)
     if weights is not None:
         layer.prepare_weights({k: v.to(device).contiguous() for k, v in weights.items()})
     torch.cuda.synchronize()

@@ -1,6 +1,8 @@
 """Parity at the full workload sizes, in the launch configuration the
 benchmark times (one layer created for T tokens, one forward), on sampled
-outputs the oracle computes one token at a time (GPU).
+outputs the oracle computes one token at a time (GPU).  The 32K-token prefill is the
+one size where the bf16 GEMM2 output passes 2^31 bytes and the two-pass
+expert scan runs over 4,096 routing blocks.
 
 At full size the whole routing is still checked bit-exactly (top-k ids,
 per-expert offsets, the permutation); the GEMM1 activation quantisation and
@@ -18,7 +20,8 @@ from tests.gpu_helpers import TOL, bf16_bits_to_f64, cfg_of, make_layer, rel_l2
 pytestmark = pytest.mark.gpu
 
 FULL = [("bf16", None), ("mxfp8_decode", None), ("nvfp4_decode", 1), ("nvfp4_decode", 8),
-        ("nvfp4_decode", 32), ("nvfp4_decode", 128), ("nvfp4_prefill", None)]
+        ("nvfp4_decode", 32), ("nvfp4_decode", 128), ("nvfp4_prefill", None),
+        ("nvfp4_prefill_32k", None)]
 
 
 def _sample(T, n=5, seed=0):

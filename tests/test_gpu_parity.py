@@ -207,11 +207,11 @@ def test_allocation_failure_reports_oom_and_frees(monkeypatch):
     torch.cuda.synchronize()
     free0 = torch.cuda.mem_get_info()[0]
     for n in (1, 5, 12):
-        monkeypatch.setenv("MOE_TEST_FAIL_ALLOC_AT", str(n))
         with pytest.raises(MoEError) as e:
-            moe_create(512, 1024, 512, 16, 4, "nvfp4")
+            moe_create(512, 1024, 512, 16, 4, "nvfp4", test_fail_alloc_at=n)
         assert e.value.code == 5
-    monkeypatch.delenv("MOE_TEST_FAIL_ALLOC_AT")
+    # the environment does not inject faults: only the config field does
+    monkeypatch.setenv("MOE_TEST_FAIL_ALLOC_AT", "1")
     h = moe_create(512, 1024, 512, 16, 4, "nvfp4")
     moe_destroy(h)
     torch.cuda.synchronize()

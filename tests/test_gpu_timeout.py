@@ -1,6 +1,6 @@
 """Bounded device waits (GPU): a GEMM whose data never arrives gives up.
 
-The test hook MOE_TEST_STALL_GEMM=1 (read when a layer is created) makes one
+The fault-injection field moe_config.test_stall_gemm = 1 makes one
 CTA of every GEMM1 launch leave one stage of its shared-memory ring unloaded,
 so the barrier waits on that stage are never satisfied (in the narrow kernel
 and in the 16-warp wide NVFP4 kernel).  Each wait gives up
@@ -29,8 +29,7 @@ def test_gemm_wait_runs_out_and_is_reported(wide, monkeypatch):
         monkeypatch.setenv("MOE_WIDE_TILES", "1")
     s = workloads.spec("nvfp4_small")
     case = workloads.make_case(s, seed=21)
-    monkeypatch.setenv("MOE_TEST_STALL_GEMM", "1")
-    layer = make_layer(s, weights=case["weights"])
+    layer = make_layer(s, weights=case["weights"], test_stall_gemm=1)
     t0 = time.perf_counter()
     run_gpu(layer, case["hidden"], case["logits"])
     waited = time.perf_counter() - t0
@@ -39,8 +38,7 @@ def test_gemm_wait_runs_out_and_is_reported(wide, monkeypatch):
     assert 1.5 < waited < 60.0, waited
     layer.close()
 
-    # the context is intact: a layer without the hook computes correctly
-    monkeypatch.delenv("MOE_TEST_STALL_GEMM")
+    # the context is intact: a layer without the fault injection computes correctly
     layer = make_layer(s, weights=case["weights"])
     out = run_gpu(layer, case["hidden"], case["logits"])
     assert layer.status() == 0

@@ -6,14 +6,16 @@ allocation may cause.  moe_route_permute_static serves them: its scratch is
 a fixed array inside the library.  This test calls it through the C ABI
 twice in a row (different sizes, so stale scratch contents from the first
 call would show) and checks each result against the regular entry point's
-routing (moe_forward + moe_debug_routing): ids, offsets and permutation
-bit-exact, routing weights within 1e-6.  It lives in a file of its own that
-pytest collects last.
+routing (moe_forward + moe_debug_routing) and against the oracle, at the
+sizes the fixed array is built for (T = 4096, E = 512, K = 16) too: ids,
+offsets and permutation bit-exact, routing weights within 1e-6.  It lives in
+a file of its own that pytest collects last.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -54,6 +56,26 @@ def test_static_routing_matches_regular_entry_point_twice():
         assert np.max(np.abs(got[1] - ref[1])) <= 1e-6
         assert np.array_equal(got[2], ref[2])
         assert np.array_equal(got[3], ref[3])
+
+
+def _check_vs_oracle(got, logits, K, E):
+    lg = logits.cpu().numpy()
+    ids_ref, w_ref = oracle.route(lg, K)
+    off_ref, perm_ref, _ = oracle.permute(ids_ref, E)
+    assert np.array_equal(got[0], ids_ref)
+    assert np.max(np.abs(got[1] - w_ref)) <= 1e-6
+    assert np.array_equal(got[2], off_ref)
+    assert np.array_equal(got[3], perm_ref)
+
+
+def test_static_routing_at_its_limits_matches_oracle_twice():
+    # T = 4096 (64 routing blocks, the array's capacity), E = 512 (16 logits
+    # per lane), K = 16; then a smaller call on the same array
+    for T, E, K, seed in ((4096, 512, 16, 1), (70, 40, 6, 2), (4096, 512, 16, 3)):
+        g = torch.Generator().manual_seed(seed)
+        logits = torch.randn(T, E, generator=g).cuda()
+        got = _static_routing(T, E, K, logits)
+        _check_vs_oracle(got, logits, K, E)
 
 
 def test_static_routing_rejects_sizes_beyond_its_scratch():
