@@ -265,6 +265,11 @@ moe_status moe_timing_stop(moe_layer *layer, float *kernel_ms, int *forwards);
  * own call).                                                              */
 int moe_last_launch_count(const moe_layer *layer);
 
+/* Largest number of CTAs a GEMM launch of this layer uses (the build's own
+ * call): wide != 0 for the prefill-sized launches (NVFP4: CTA pairs, two
+ * CTAs each), 0 for the others.  0 for a NULL handle.                    */
+int moe_gemm_ctas(const moe_layer *layer, int wide);
+
 /* Routing and expert permutation without any device allocation.  The pages
  * have no counterpart of this entry point; it exists for callers that cannot
  * call cudaMalloc -- e.g. a serving framework whose caching allocator

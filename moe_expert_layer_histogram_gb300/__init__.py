@@ -45,6 +45,7 @@ EXPORTS = ("moe_create", "moe_prepare_weights", "moe_forward", "moe_forward_batc
            "moe_debug_routing", "moe_debug_act_quant", "moe_debug_intermediates",
            "moe_debug_weight_tiles",
            "moe_get_status", "moe_timing_start", "moe_timing_stop", "moe_last_launch_count",
+           "moe_gemm_ctas",
            "moe_route_permute_static", "moe_measure_mma_rate", "moe_status_string",
            "moe_destroy")
 
@@ -73,6 +74,7 @@ def lib():
     L.moe_timing_start.argtypes = [vp, ci]
     L.moe_timing_stop.argtypes = [vp, vp, vp]
     L.moe_last_launch_count.argtypes = [vp]
+    L.moe_gemm_ctas.argtypes = [vp, ci]
     L.moe_route_permute_static.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp, vp]
     L.moe_measure_mma_rate.argtypes = [ci, ci, ci, ci, ctypes.POINTER(ctypes.c_double), vp]
     L.moe_status_string.argtypes = [ci]
@@ -182,6 +184,10 @@ def moe_timing_stop(handle):
 
 def moe_last_launch_count(handle):
     return lib().moe_last_launch_count(handle)
+
+
+def moe_gemm_ctas(handle, wide):
+    return lib().moe_gemm_ctas(handle, int(bool(wide)))
 
 
 def moe_route_permute_static(router_logits, T, E, K, topk_ids, topk_w, offsets, perm,

@@ -14,7 +14,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmoe_gb300.so")
-SOURCES = ["gemm.cu", "route.cu", "prep.cu", "api.cu", "route_static.cu", "peak.cu"]
+SOURCES = ["gemm.cu", "gemm_pair.cu", "decode.cu", "route.cu", "prep.cu", "api.cu",
+           "route_static.cu", "peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -45,6 +45,8 @@ struct moe_layer {
   float* acc = nullptr;              // in-kernel reduce: fp32 [Tmax, H], zero between forwards
   int32_t *acc_cnt = nullptr, *prow_slot = nullptr;
   int32_t* done1 = nullptr;          // fused decode GEMMs: per-expert GEMM1 completion counts
+  DecodeCtl* dctl = nullptr;         // single-launch decode: counters (zero between forwards)
+  int single_launch = 1;             // T <= 16: the whole layer in one kernel
   int fused_gemms = 1;               // T <= 16: GEMM1 and GEMM2 in one launch
   int host_zero_copy = 1;            // moe_forward_host: kernels access pinned host buffers
   float* w = nullptr;
@@ -59,6 +61,7 @@ struct moe_layer {
   int stage_scales = 1;              // decode scales written by a warp, not copied
   int test_stall = 0;                // fault injection (moe_config.test_stall_gemm): GEMM1 times out
   int max_ctas = 0;                  // CTAs per GEMM launch (moe_config.max_ctas, else the SM count)
+  int pair_clusters = 0;             // NVFP4 wide launches: co-resident CTA pairs (0: single CTAs)
   bool weights_ready = false;
   int last_T = 0, last_launches = 0;
   std::vector<cudaEvent_t> tev;  // per-kernel timing events, 7 per forward
@@ -203,22 +206,34 @@ GemmArgs gemm2_args(const moe_layer* L, int pair, bool wide, void* out, int rows
   return a;
 }
 
+// Wide NVFP4 items run on CTA pairs when the device has them: one launch of
+// `clusters` pairs, each item covering up to two 128-row chunks.
+cudaError_t launch_wide_or_pair(moe_layer* L, int epi, const GemmMaps& maps, const GemmArgs& a,
+                                int64_t chunks, int max_rows, bool wide, cudaStream_t s) {
+  if (wide && L->pair_clusters > 0) {
+    const int clusters = static_cast<int>(
+        std::min<int64_t>(std::min(L->pair_clusters, std::max(1, L->max_ctas / 2)),
+                          (chunks + 1) / 2 * a.n_tiles));
+    return launch_gemm_pair(epi, maps, a, clusters, s);
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(L->max_ctas, chunks * a.n_tiles));
+  return launch_gemm(L->fmt, epi, maps, a, grid, max_rows, wide, s);
+}
+
 // max_rows bounds the rows of any expert (selects the activation tile height).
 cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide,
                       cudaStream_t s) {
   wide = wide && L->w13_rows % 256 == 0;
   const GemmArgs a = gemm1_args(L, pair, wide);
-  const int grid = static_cast<int>(std::min<int64_t>(L->max_ctas, chunks * a.n_tiles));
-  return launch_gemm(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a, grid, max_rows, wide,
-                     s);
+  return launch_wide_or_pair(L, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a, chunks, max_rows,
+                             wide, s);
 }
 
 cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide, void* out,
                       int rows_per_expert, cudaStream_t s, void* reduce_out = nullptr) {
   wide = wide && L->H % 256 == 0;
   const GemmArgs a = gemm2_args(L, pair, wide, out, rows_per_expert, reduce_out);
-  const int grid = static_cast<int>(std::min<int64_t>(L->max_ctas, chunks * a.n_tiles));
-  return launch_gemm(L->fmt, 2, L->maps2, a, grid, max_rows, wide, s);
+  return launch_wide_or_pair(L, 2, L->maps2, a, chunks, max_rows, wide, s);
 }
 
 // Decode: GEMM1 and GEMM2 in one persistent launch (narrow items, chunks of
@@ -341,6 +356,24 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   // up after 2 s and moe_get_status reports MOE_ERR_DEVICE_TIMEOUT.
   L->test_stall = c.test_stall_gemm == 1;
   L->max_ctas = c.max_ctas > 0 ? std::min(c.max_ctas, sms) : sms;
+  // NVFP4 wide (prefill) launches on CTA pairs with MOE_PAIR_CTAS=1 (off by
+  // default: measured slower than single CTAs so far).
+  if (L->fmt == MOE_FMT_NVFP4) {
+    const char* pv2 = std::getenv("MOE_PAIR_CTAS");
+    if (pv2 && pv2[0] == '1' && gemm_pair_prepare(&L->pair_clusters) != cudaSuccess) {
+      cudaGetLastError();
+      delete L;
+      return MOE_ERR_NO_DEVICE;
+    }
+  }
+  // MOE_SINGLE_LAUNCH=0: decode batches use the three-launch path (front
+  // end, both GEMMs in one launch, combine) instead of the single kernel.
+  if (const char* sv1 = std::getenv("MOE_SINGLE_LAUNCH")) L->single_launch = sv1[0] != '0';
+  if (decode_prepare(L->fmt) != cudaSuccess) {
+    cudaGetLastError();
+    delete L;
+    return MOE_ERR_NO_DEVICE;
+  }
   // MOE_FUSED_GEMMS=0: decode launches keep GEMM1 and GEMM2 separate.
   if (const char* fv = std::getenv("MOE_FUSED_GEMMS")) L->fused_gemms = fv[0] != '0';
   // MOE_HOST_ZERO_COPY=0: moe_forward_host always copies through device buffers.
@@ -374,7 +407,8 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
             A.get(&L->h_in, static_cast<size_t>(L->Tmax) * H * 2) &&
             A.get(&L->l_in, static_cast<size_t>(L->Tmax) * E * 4) &&
             A.get(&L->o_out, static_cast<size_t>(L->Tmax) * H * 2) &&
-            A.get(&L->done1, static_cast<size_t>(E) * 4);
+            A.get(&L->done1, static_cast<size_t>(E) * 4) &&
+            A.get(&L->dctl, sizeof(DecodeCtl));
   const bool reduce = L->combine == MOE_COMBINE_REDUCE;
   ok = ok && (!reduce || (A.get(&L->acc, static_cast<size_t>(L->Tmax) * H * 4) &&
                           A.get(&L->acc_cnt, static_cast<size_t>(L->Tmax) * (H / 128) * 4) &&
@@ -389,6 +423,7 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
        cudaMemset(L->hq, 0, static_cast<size_t>(Rpad) * L->hb) == cudaSuccess &&
        cudaMemset(L->y, 0, static_cast<size_t>(Rpad) * H * 2) == cudaSuccess &&
        cudaMemset(L->status, 0, 16) == cudaSuccess &&
+       cudaMemset(L->dctl, 0, sizeof(DecodeCtl)) == cudaSuccess &&
        (!reduce || (cudaMemset(L->acc, 0, static_cast<size_t>(L->Tmax) * H * 4) == cudaSuccess &&
                     cudaMemset(L->acc_cnt, 0, static_cast<size_t>(L->Tmax) * (H / 128) * 4) ==
                         cudaSuccess));
@@ -457,6 +492,45 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   cudaError_t e;
   int launches = 4;
   const bool small = T <= kSmallFrontTokens;
+  if (small && L->single_launch && L->fused_gemms && L->combine == MOE_COMBINE_GATHER &&
+      (L->stage_scales || L->fmt == MOE_FMT_BF16)) {
+    // the whole layer in one launch (timed as GEMM1)
+    GemmArgs a1 = gemm1_args(L, 1, false);
+    const GemmArgs a2 = gemm2_args(L, 1, false, L->y, 0, nullptr);
+    DecodeArgs d{};
+    d.logits = logits;
+    d.hidden = hidden;
+    d.T = T;
+    d.K = K;
+    d.H = H;
+    d.ids = L->ids;
+    d.counts = L->counts;
+    d.offsets = L->offsets;
+    d.pad_off = L->pad_off;
+    d.chunk_off = L->chunk_off;
+    d.perm = L->perm;
+    d.inv = L->inv;
+    d.w = L->w;
+    d.xq = L->xq;
+    d.xsf = L->xsf;
+    d.out = static_cast<uint8_t*>(out);
+    d.ctl = L->dctl;
+    const int64_t chunks = max_chunks(L, T);
+    const int grid = static_cast<int>(
+        std::min<int64_t>(L->max_ctas, chunks * (a1.n_tiles + a2.n_tiles)));
+    mark(1);
+    mark(2);
+    mark(3);
+    e = launch_decode(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a1, L->maps2, a2, d,
+                      grid, s);
+    mark(4);
+    mark(5);
+    mark(6);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    L->last_T = T;
+    L->last_launches = 1;
+    return MOE_OK;
+  }
   if (small) {
     // one kernel for routing .. GEMM1 input (timed as the routing kernel)
     e = launch_small_front(L->fmt, logits, T, E, K, hidden, H, L->ids, L->w, L->counts,
@@ -671,6 +745,13 @@ moe_status moe_timing_stop(moe_layer* L, float* kernel_ms, int* forwards) {
 }
 
 int moe_last_launch_count(const moe_layer* L) { return L ? L->last_launches : 0; }
+
+int moe_gemm_ctas(const moe_layer* L, int wide) {
+  if (!L) return 0;
+  if (wide && L->pair_clusters > 0)
+    return 2 * std::min(L->pair_clusters, std::max(1, L->max_ctas / 2));
+  return L->max_ctas;
+}
 
 void moe_destroy(moe_layer* L) {
   if (!L) return;

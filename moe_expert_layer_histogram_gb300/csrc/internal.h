@@ -126,6 +126,47 @@ cudaError_t launch_gemm_fused(int fmt, int epi1, const GemmMaps& maps1, const Ge
                               const GemmMaps& maps2, const GemmArgs& args2, int grid,
                               int max_rows, cudaStream_t s);
 
+// NVFP4 wide launches on CTA pairs (tcgen05 cta_group::2, 256 x 256 MMA
+// tiles): prepare once (sets the shared-memory limit, checks the register
+// split, returns the largest number of co-resident CTA pairs); launch with
+// `clusters` pairs (args as for wide items: n_tiles counts 256-row pairs).
+cudaError_t gemm_pair_prepare(int* max_clusters);
+cudaError_t launch_gemm_pair(int epi, const GemmMaps& maps, const GemmArgs& args, int clusters,
+                             cudaStream_t s);
+
+// Single-launch decode layer (T <= kSmallFrontTokens): routing, tables,
+// GEMM1 input, both GEMMs and the combine in one persistent kernel.  The
+// counters below coordinate its CTAs; they are zero between forwards (the
+// kernel's last CTA resets them).
+struct DecodeCtl {
+  int qclaim, qdone;    // GEMM1-input tokens claimed / stored
+  int iclaim;           // GEMM items claimed
+  int cclaim;           // combine units claimed
+  int exits;            // CTAs finished
+  int pad[3];
+  int done1[kMaxExperts];  // per expert: GEMM1 epilogue warps finished
+  int done2[kMaxExperts];  // per expert: GEMM2 epilogue warps finished
+};
+
+struct DecodeArgs {
+  const float* logits;   // [T, E]
+  const void* hidden;    // bf16 [T, H]
+  int T, K, H;
+  // routing tables (written by CTA 0, for inspection)
+  int32_t *ids, *counts, *offsets, *pad_off, *chunk_off, *perm, *inv;
+  float* w;
+  uint8_t *xq, *xsf;     // GEMM1 input rows and their scale tiles
+  uint8_t* out;          // bf16 [T, H]
+  DecodeCtl* ctl;
+};
+
+cudaError_t decode_prepare(int fmt);
+// args1/args2: GEMM1 / GEMM2 arguments as for launch_gemm (narrow items;
+// their table pointers are not read: the kernel builds the tables itself).
+cudaError_t launch_decode(int fmt, int epi1, const GemmMaps& maps1, const GemmArgs& args1,
+                          const GemmMaps& maps2, const GemmArgs& args2, const DecodeArgs& d,
+                          int grid, cudaStream_t s);
+
 // Routing, permutation + activation quantisation, combine.
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* w,
                          int32_t* blockhist, cudaStream_t s);

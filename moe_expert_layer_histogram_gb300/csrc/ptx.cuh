@@ -383,4 +383,87 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
                  "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 
+// ---------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs (ranks 0 and 1) shares one tcgen05 MMA
+// (cta_group::2): rank 0 issues it, each CTA supplies its own operand halves
+// from its own shared memory and receives its half of the result in its own
+// TMEM.  Barriers a CTA waits on may be arrived on from the peer CTA.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs: release this CTA's earlier writes (shared
+// memory, barrier initialisation) to the peer and wait for the peer.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Arrive on the barrier at `bar`'s offset in CTA `rank` (this CTA or its
+// peer).  Default (CTA-scope release) semantics: what the arrive announces --
+// TMEM stores completed by tcgen05.wait::st, TMEM loads completed by
+// tcgen05.wait::ld, shared-memory data whose copies completed -- is already
+// in place, and a cluster-scope release would also wait for this thread's
+// outstanding global stores (measured: the pair kernels ran at half speed,
+// stalled on memory barriers).
+__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(
+                   mapa_shared(smem_u32(bar), rank))
+               : "memory");
+}
+
+// TMEM of a CTA pair: one warp of each CTA executes these together; both
+// CTAs receive the same columns.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Arrive on the barrier at `bar`'s offset in every CTA of `cta_mask` once the
+// pair MMAs this thread issued so far have completed.
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// 256 x N block-scaled NVFP4 MMA of a CTA pair (issued by rank 0): rows
+// 0-127 of A and of D in rank 0, rows 128-255 in rank 1; B rows 0..N/2-1
+// from rank 0's shared memory and N/2..N-1 from rank 1's; each CTA reads its
+// rows' A scales and all N rows' B scales from its own TMEM, in the layout of
+// the single-CTA MMA.
+__device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                              uint32_t idesc, uint32_t sfa_tmem,
+                                              uint32_t sfb_tmem, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accum)
+      : "memory");
+}
+
 }  // namespace moe

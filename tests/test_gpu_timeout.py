@@ -21,12 +21,15 @@ pytestmark = pytest.mark.gpu
 MOE_ERR_DEVICE_TIMEOUT = 6
 
 
-@pytest.mark.parametrize("wide", [False, True], ids=["narrow", "wide"])
-def test_gemm_wait_runs_out_and_is_reported(wide, monkeypatch):
+@pytest.mark.parametrize("wide,pairs", [(False, False), (True, False), (True, True)],
+                         ids=["narrow", "wide", "wide-pairs"])
+def test_gemm_wait_runs_out_and_is_reported(wide, pairs, monkeypatch):
     # wide: the 16-warp NVFP4 kernel, whose scale-stager warps are the ones
-    # waiting on the stage that never lands
+    # waiting on the stage that never lands; pairs: the CTA-pair kernel, where
+    # the stalled CTA's peer gives up its own waits on the shared MMA too
     if wide:
         monkeypatch.setenv("MOE_WIDE_TILES", "1")
+        monkeypatch.setenv("MOE_PAIR_CTAS", "1" if pairs else "0")
     s = workloads.spec("nvfp4_small")
     case = workloads.make_case(s, seed=21)
     layer = make_layer(s, weights=case["weights"], test_stall_gemm=1)
