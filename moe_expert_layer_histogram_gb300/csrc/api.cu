@@ -84,8 +84,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D byte tensor [rows, row_bytes], box of 128 bytes x box_rows, 128-byte
-// swizzle (the layout the MMA descriptors expect).
-bool make_map(CUtensorMap* m, void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+// swizzle (the layout the MMA descriptors expect) or none (data stored
+// pre-swizzled).
+bool make_map(CUtensorMap* m, void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows,
+              bool swizzle = true) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {row_bytes, rows};
@@ -93,7 +95,22 @@ bool make_map(CUtensorMap* m, void* base, uint64_t row_bytes, uint64_t rows, uin
   cuuint32_t box[2] = {128, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Prepared weight tiles viewed as rows of 2 KiB (256 x 64-bit elements), box
+// of 8 rows (16 KiB), no swizzle: the codes are stored pre-swizzled.
+bool make_tile_map(CUtensorMap* m, void* base, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {256, rows};
+  cuuint64_t strides[1] = {2048};
+  cuuint32_t box[2] = {256, 8};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -431,6 +448,16 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
     ok = make_map(&L->maps1.a[i], L->xq, L->xb, Rpad, 16u << i) &&
          make_map(&L->maps2.a[i], L->hq, L->hb, Rpad, 16u << i);
   }
+  // NVFP4 weight tiles (18 KiB: 16 KiB of codes, 2 KiB of scales) as rows
+  // of 2 KiB: the codes of tile t are rows 9t .. 9t+7, one box of 8 rows
+  if (L->fmt == MOE_FMT_NVFP4)
+    ok = ok &&
+         make_tile_map(&L->maps1.b, L->w13t,
+                       static_cast<uint64_t>(E) * (L->w13_rows / 128) * (L->xb / 128) *
+                           weight_tile_bytes(L->fmt) / 2048) &&
+         make_tile_map(&L->maps2.b, L->w2t,
+                       static_cast<uint64_t>(E) * (H / 128) * (L->hb / 128) *
+                           weight_tile_bytes(L->fmt) / 2048);
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();

@@ -135,6 +135,12 @@ __device__ __forceinline__ bool wait_counter(const int* counter, int need, volat
   return wait_count_at_least(counter, need, abort);
 }
 
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -401,24 +407,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const uint8_t* btile =
             A.b_tiles + (static_cast<int64_t>(it.e) * A.n_tiles + it.n_tile) * A.num_kb *
                             A.b_tile_bytes;
-        const bool must_wait = second(item) || !a_ready;
-        if (must_wait) {
-          // start the weight stream before waiting for the activations
-          for (int kb = 0; kb < A.num_kb; ++kb)
-            prefetch_l2(btile + static_cast<int64_t>(kb) * A.b_tile_bytes, A.b_tile_bytes);
-          bool got;
-          if (second(item)) {
-            // GEMM2's activations are GEMM1's output for this expert
-            const int need = 4 * a1.n_tiles * (tab.chunk_off[it.e + 1] - tab.chunk_off[it.e]);
-            got = wait_counter(ctl->done1 + it.e, need, abort_flag);
-          } else {
-            got = wait_counter(&ctl->qdone, T, abort_flag);
-            a_ready = got;
+        if (second(item) || !a_ready) {
+          // GEMM2's activations are GEMM1's output for this expert; GEMM1's
+          // are the quantised tokens
+          const int* counter = second(item) ? ctl->done1 + it.e : &ctl->qdone;
+          const int need =
+              second(item) ? 4 * a1.n_tiles * (tab.chunk_off[it.e + 1] - tab.chunk_off[it.e]) : T;
+          if (ld_acquire(counter) < need) {
+            // start the weight stream before waiting for the activations
+            for (int kb = 0; kb < A.num_kb; ++kb)
+              prefetch_l2(btile + static_cast<int64_t>(kb) * A.b_tile_bytes, A.b_tile_bytes);
+            if (!wait_counter(counter, need, abort_flag)) {
+              ok = false;
+              break;
+            }
           }
-          if (!got) {
-            ok = false;
-            break;
-          }
+          if (!second(item)) a_ready = true;
           fence_proxy_async_global();  // generic-proxy stores -> the TMA reads below
         }
         for (int kb = 0; kb < A.num_kb; ++kb) {

@@ -67,6 +67,9 @@ struct GemmArgs {
 
 struct GemmMaps {
   CUtensorMap a[4];  // activation rows, boxes of 16/32/64/128 rows x 128 B
+  CUtensorMap b;     // NVFP4 prepared weight tiles as rows of 2 KiB, boxes of 8 rows (a
+                     // tile's 16 KiB of codes), no swizzle (stored pre-swizzled);
+                     // CTA-pair kernels
 };
 
 // Prepared weights are stored as tiles, one per (expert, 128-row block of

@@ -449,6 +449,19 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask)
       : "memory");
 }
 
+// TMA tensor load into this CTA's shared memory whose completion is
+// signalled on an mbarrier of either CTA of the pair (`bar_cluster`: a
+// shared::cluster address, e.g. from mapa_shared).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
 // 256 x N block-scaled NVFP4 MMA of a CTA pair (issued by rank 0): rows
 // 0-127 of A and of D in rank 0, rows 128-255 in rank 1; B rows 0..N/2-1
 // from rank 0's shared memory and N/2..N-1 from rank 1's; each CTA reads its

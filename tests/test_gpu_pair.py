@@ -1,7 +1,7 @@
 """NVFP4 prefill GEMMs on CTA pairs (GPU).
 
-Wide NVFP4 launches run on clusters of two CTAs sharing one 256 x 256 MMA
-(tcgen05 cta_group::2): CTA r of a pair loads token chunk 2c + r and weight
+Wide NVFP4 launches can run on clusters of two CTAs sharing one 256 x 256
+MMA (tcgen05 cta_group::2; MOE_PAIR_CTAS=1): CTA r of a pair loads token chunk 2c + r and weight
 tile 2n + r.  These cases check the pair kernels against the oracle and
 against the single-CTA wide kernels (MOE_PAIR_CTAS=0) on the same inputs:
 experts with an odd number of chunks (the second CTA of the last pair has
@@ -79,6 +79,7 @@ def test_pair_kernels_in_kernel_reduce(monkeypatch):
 
 def test_pair_kernels_batched_format(monkeypatch):
     monkeypatch.setenv("MOE_WIDE_TILES", "1")
+    monkeypatch.setenv("MOE_PAIR_CTAS", "1")
     s = workloads.spec("nvfp4_small", E=5)
     M = 300
     case = workloads.make_case(s, T=1, seed=73)
@@ -105,6 +106,7 @@ def test_pair_kernels_with_few_ctas(monkeypatch):
     case = workloads.make_case(s, seed=79)
     ref = run_oracle(s, case)
     monkeypatch.setenv("MOE_WIDE_TILES", "1")
+    monkeypatch.setenv("MOE_PAIR_CTAS", "1")
     layer = make_layer(s, weights=case["weights"], max_ctas=4)
     out = run_gpu(layer, case["hidden"], case["logits"])
     assert layer.status() == 0
