@@ -8,8 +8,8 @@
 //      128-row-padded offsets, chunk offsets, stable ranks) -- every CTA
 //      computes them itself in shared memory (T <= 16 tokens, a few hundred
 //      experts), CTA 0 also stores them for inspection;
-//   2. the GEMM1 input of each token, quantised into its K padded rows by
-//      whichever CTA claims that token (an atomic counter);
+//   2. the GEMM1 input of each token, quantised into its K padded rows in
+//      row segments, each by whichever CTA claims it (an atomic counter);
 //   3. the GEMM1 (+ SwiGLU or squared ReLU, re-quantised) and GEMM2 work
 //      items, claimed one at a time from an atomic counter in order (all
 //      GEMM1 items before any GEMM2 item); a GEMM2 item of expert e waits
@@ -61,6 +61,7 @@ struct DecSmem {
   int ids[kSmallFrontTokens * kMaxTopK];
   float w[kSmallFrontTokens * kMaxTopK];
   int prow[kSmallFrontTokens * kMaxTopK];
+  int rank2[kSmallFrontTokens * kMaxTopK];
   int wsum[3 * kDecWarps];
   int items[kItemRing];
   int bcast;
@@ -207,11 +208,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   int* counts = S.tab + 2 * E + 1;
   for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = S.rank[e] = 0;
   __syncthreads();
-  // the previous forward's kernels may still read what this one writes, and
-  // a layer's inputs may be the previous layer's output
-  pdl_wait();
 
   // ---------------------------------------------------------------- 1. routing, tables
+  // Routing reads only the router logits, which the layer's own kernels never
+  // write (the router GEMM producing them is not launched with programmatic
+  // dependencies), so it runs before the wait on the previous kernel, like
+  // the multi-kernel path's routing kernel; everything it writes to global
+  // memory waits.
   for (int t = warp; t < T; t += kDecWarps) {
     int my_i;
     float my_w;
@@ -235,17 +238,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int s = t * K + lane;
         const int e = S.ids[s];
         const int r = S.rank[e]++;
-        const int prow = pad_off[e] + r;
-        S.prow[s] = prow;
-        if (store_tables) {
-          d.perm[S.off[e] + r] = s;
-          d.inv[s] = prow;
-        }
+        S.prow[s] = pad_off[e] + r;
+        S.rank2[s] = S.off[e] + r;  // unpadded row, for the permutation table
       }
       __syncwarp();
     }
   }
+  __syncthreads();
+  // the previous forward's kernels may still read what this one writes, and
+  // a layer's hidden states may be the previous layer's output
+  pdl_wait();
   if (store_tables) {
+    for (int i = threadIdx.x; i < T * K; i += blockDim.x) {
+      d.perm[S.rank2[i]] = i;
+      d.inv[i] = S.prow[i];
+    }
     for (int i = threadIdx.x; i < T * K; i += blockDim.x) {
       d.ids[i] = S.ids[i];
       d.w[i] = S.w[i];
@@ -263,15 +270,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
 
   // ---------------------------------------------------------------- 2. GEMM1 input
+  // Work units are row segments of kDecThreads quantisation blocks (one per
+  // thread), claimed in order, so a token's row is spread over several CTAs.
+  const int segs = (row_units<FMT>(H) + kDecThreads - 1) / kDecThreads;  // segments per token
   for (;;) {
     if (threadIdx.x == 0) S.bcast = atomicAdd(&ctl->qclaim, 1);
     __syncthreads();
     const int u = S.bcast;
     __syncthreads();
-    if (u >= T) break;
-    for (int unit = threadIdx.x; unit < row_units<FMT>(H); unit += blockDim.x)
-      quant_unit_to_rows<FMT>(static_cast<const __nv_bfloat16*>(d.hidden) + static_cast<int64_t>(u) * H,
-                              H, unit, S.prow + u * K, K, d.xq, d.xsf);
+    if (u >= T * segs) break;
+    const int t = u / segs;
+    const int unit = (u - t * segs) * kDecThreads + threadIdx.x;
+    if (unit < row_units<FMT>(H))
+      quant_unit_to_rows<FMT>(static_cast<const __nv_bfloat16*>(d.hidden) + static_cast<int64_t>(t) * H,
+                              H, unit, S.prow + t * K, K, d.xq, d.xsf);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) atomicAdd(&ctl->qdone, 1);
@@ -412,7 +424,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           // are the quantised tokens
           const int* counter = second(item) ? ctl->done1 + it.e : &ctl->qdone;
           const int need =
-              second(item) ? 4 * a1.n_tiles * (tab.chunk_off[it.e + 1] - tab.chunk_off[it.e]) : T;
+              second(item) ? 4 * a1.n_tiles * (tab.chunk_off[it.e + 1] - tab.chunk_off[it.e])
+                         : T * segs;
           if (ld_acquire(counter) < need) {
             // start the weight stream before waiting for the activations
             for (int kb = 0; kb < A.num_kb; ++kb)
