@@ -9,16 +9,29 @@
 // report, sec. 实现拆解 item 1).
 #pragma once
 
-#include <cfloat>
-#include <climits>
 #include <cstdint>
 
 namespace moe {
 
-// Lane l holds logits l, l+32, ... (MAXJ of them, E <= 32 MAXJ); K rounds of
-// a warp arg-max in the total order, then the softmax of the K selected
-// values.  Lane k < K receives the k-th expert in *id and its softmax weight
-// in *wt; the other lanes receive weight 0.
+// Order-preserving 32-bit key of a router logit: larger value -> larger
+// key, -0.0 and +0.0 the same key, every finite or infinite value >= 1 (0
+// marks an empty slot).  NaN logits are not supported.
+__device__ __forceinline__ uint32_t logit_key(float x) {
+  uint32_t b = __float_as_uint(x);
+  if (b == 0x80000000u) b = 0u;  // -0.0 == +0.0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Lane l holds logits l, l+32, ... (MAXJ of them, E <= 32 MAXJ).  Each of
+// the K rounds takes the warp's largest key (redux.sync max), then the
+// lowest expert index holding it (redux.sync min), and removes that entry;
+// then the softmax of the K selected values.  Lane k < K receives the k-th
+// expert in *id and its softmax weight in *wt; the other lanes receive
+// weight 0.
 template <int MAXJ>
 __device__ __forceinline__ void route_token(const float* __restrict__ l, int E, int K, int lane,
                                             int* id, float* wt) {
@@ -26,40 +39,30 @@ __device__ __forceinline__ void route_token(const float* __restrict__ l, int E, 
   float my_v = 0.0f;
   int my_i = 0;
   {
-    float v[MAXJ];
-    uint32_t avail = 0;
+    uint32_t key[MAXJ];
 #pragma unroll
     for (int j = 0; j < MAXJ; ++j) {
       const int e = lane + 32 * j;
-      v[j] = -FLT_MAX;
-      if (e < E) {
-        v[j] = __ldg(l + e);
-        avail |= 1u << j;
-      }
+      key[j] = e < E ? logit_key(__ldg(l + e)) : 0u;
     }
     for (int k = 0; k < K; ++k) {
-      float bv = -FLT_MAX;
-      int bi = INT_MAX;
+      uint32_t m = 0u;
 #pragma unroll
-      for (int j = 0; j < MAXJ; ++j)
-        if (((avail >> j) & 1u) && (bi == INT_MAX || v[j] > bv)) {
-          bv = v[j];
-          bi = lane + 32 * j;
-        }
+      for (int j = 0; j < MAXJ; ++j) m = max(m, key[j]);
+      const uint32_t wmax = __reduce_max_sync(kAll, m);
+      uint32_t idx = 0xFFFFFFFFu;
 #pragma unroll
-      for (int off = 16; off; off >>= 1) {
-        const float ov = __shfl_xor_sync(kAll, bv, off);
-        const int oi = __shfl_xor_sync(kAll, bi, off);
-        const bool take = oi != INT_MAX && (bi == INT_MAX || ov > bv || (ov == bv && oi < bi));
-        if (take) {
-          bv = ov;
-          bi = oi;
-        }
+      for (int j = MAXJ - 1; j >= 0; --j)
+        if (key[j] == wmax) idx = static_cast<uint32_t>(lane + 32 * j);
+      const uint32_t widx = __reduce_min_sync(kAll, idx);
+      if (static_cast<int>(widx & 31u) == lane) {
+#pragma unroll
+        for (int j = 0; j < MAXJ; ++j)
+          if (static_cast<uint32_t>(j) == (widx >> 5)) key[j] = 0u;
       }
-      if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
       if (lane == k) {
-        my_v = bv;
-        my_i = bi;
+        my_v = key_logit(wmax);
+        my_i = static_cast<int>(widx);
       }
     }
   }
