@@ -48,9 +48,10 @@ def parse_args():
                    help="override E (small cases for profiler captures)")
     p.add_argument("--act", default="", choices=["", "swiglu", "relu2"],
                    help="expert activation (default: the workload's; relu2 drops the clamp)")
-    p.add_argument("--combine", default="gather", choices=["gather", "reduce"],
-                   help="sum of the K expert outputs: combine kernel (deterministic) or "
-                        "in-kernel atomic reduce")
+    p.add_argument("--combine", default="gather", choices=["gather", "reduce", "fused"],
+                   help="sum of the K expert outputs: combine kernel (deterministic), "
+                        "in-kernel atomic reduce, or the deterministic gather fused into "
+                        "GEMM2's epilogue")
     p.add_argument("--max-ctas", type=int, default=0,
                    help="cap on the CTAs of each GEMM launch (0: one per SM)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -77,7 +78,8 @@ def describe(s):
     return "%s: T=%d H=%d I=%d E=%d top-%d %s %s%s, logits %s%s" % (
         s["name"], s["T"], s["H"], s["I"], s["E"], s["K"], s["fmt"], s.get("act", "swiglu"),
         (", clamp %g" % s["clamp"]) if s["clamp"] else "", s["logits"],
-        ", in-kernel reduce" if s.get("combine") == "reduce" else "")
+        {"reduce": ", in-kernel reduce", "fused": ", combine fused into GEMM2"}.get(
+            s.get("combine"), ""))
 
 
 def dtype_of(s):

@@ -81,7 +81,19 @@ typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_RELU2 = 1 } moe_activation;
  * runs; the summation order, hence the last bits, can differ from run to
  * run (the in-kernel reduce the MegaMoE kernel-drop workflow page, sec. 六,
  * weighs against a deterministic combine).                                 */
-typedef enum { MOE_COMBINE_GATHER = 0, MOE_COMBINE_REDUCE = 1 } moe_combine;
+/* FUSED: the same deterministic gather as GATHER, done inside GEMM2's
+ * epilogue: in each 128-column group, the last of a token's K rows to be
+ * stored sums the token's K rows in k order in fp32 and writes the bf16
+ * result (bit-identical to GATHER), so no combine kernel runs (the combine
+ * folded into the expert GEMM, as the MegaMoE kernel fuses its FC2 with the
+ * reduction, sec. 六; here without atomics on the output).  Measured slower
+ * than GATHER on GB300 for T > 16 (the gathers lengthen GEMM2's epilogue);
+ * for T <= 16 the single-launch decode kernel's own combine is used.     */
+typedef enum {
+    MOE_COMBINE_GATHER = 0,
+    MOE_COMBINE_REDUCE = 1,
+    MOE_COMBINE_FUSED = 2
+} moe_combine;
 
 typedef struct {
     int max_tokens;    /* T_max: largest T any forward will use (>= 1)       */

@@ -17,7 +17,7 @@ LIB_PATH = _build.LIB
 
 MOE_FMT = {"bf16": 0, "mxfp8": 1, "nvfp4": 2}
 MOE_ACT = {"swiglu": 0, "relu2": 1}
-MOE_COMBINE = {"gather": 0, "reduce": 1}
+MOE_COMBINE = {"gather": 0, "reduce": 1, "fused": 2}
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_NO_WEIGHTS", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_OOM",

@@ -210,8 +210,9 @@ GemmArgs gemm2_args(const moe_layer* L, int pair, bool wide, void* out, int rows
   a.pair_scale_copies = pair;
   a.stage_scales = L->stage_scales;
   a.out_rows_per_expert = rows_per_expert;
-  if (reduce_out && L->combine == MOE_COMBINE_REDUCE) {
-    a.acc = L->acc;
+  if (reduce_out && L->combine != MOE_COMBINE_GATHER) {
+    a.acc = L->combine == MOE_COMBINE_REDUCE ? L->acc : nullptr;
+    a.gather_inv = L->combine == MOE_COMBINE_FUSED ? L->inv : nullptr;
     a.acc_cnt = L->acc_cnt;
     a.prow_slot = L->prow_slot;
     a.topk_w = L->w;
@@ -305,7 +306,9 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
     return MOE_ERR_INVALID_ARG;
   if (c.format < MOE_FMT_BF16 || c.format > MOE_FMT_NVFP4) return MOE_ERR_INVALID_ARG;
   if (c.activation != MOE_ACT_SWIGLU && c.activation != MOE_ACT_RELU2) return MOE_ERR_INVALID_ARG;
-  if (c.combine != MOE_COMBINE_GATHER && c.combine != MOE_COMBINE_REDUCE) return MOE_ERR_INVALID_ARG;
+  if (c.combine != MOE_COMBINE_GATHER && c.combine != MOE_COMBINE_REDUCE &&
+      c.combine != MOE_COMBINE_FUSED)
+    return MOE_ERR_INVALID_ARG;
   if (c.max_ctas < 0 || c.test_fail_alloc_at < 0 || c.test_stall_gemm < 0 || c.test_stall_gemm > 1)
     return MOE_ERR_INVALID_ARG;
   if (c.activation == MOE_ACT_RELU2 && c.clamp_limit > 0.0f && std::isfinite(c.clamp_limit))
@@ -427,9 +430,10 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
             A.get(&L->done1, static_cast<size_t>(E) * 4) &&
             A.get(&L->dctl, sizeof(DecodeCtl));
   const bool reduce = L->combine == MOE_COMBINE_REDUCE;
-  ok = ok && (!reduce || (A.get(&L->acc, static_cast<size_t>(L->Tmax) * H * 4) &&
-                          A.get(&L->acc_cnt, static_cast<size_t>(L->Tmax) * (H / 128) * 4) &&
-                          A.get(&L->prow_slot, static_cast<size_t>(Rpad) * 4)));
+  const bool counted = L->combine != MOE_COMBINE_GATHER;  // reduce or fused combine
+  ok = ok && (!reduce || A.get(&L->acc, static_cast<size_t>(L->Tmax) * H * 4));
+  ok = ok && (!counted || (A.get(&L->acc_cnt, static_cast<size_t>(L->Tmax) * (H / 128) * 4) &&
+                           A.get(&L->prow_slot, static_cast<size_t>(Rpad) * 4)));
   if (!ok) {
     free_all(L);
     delete L;
@@ -441,9 +445,9 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
        cudaMemset(L->y, 0, static_cast<size_t>(Rpad) * H * 2) == cudaSuccess &&
        cudaMemset(L->status, 0, 16) == cudaSuccess &&
        cudaMemset(L->dctl, 0, sizeof(DecodeCtl)) == cudaSuccess &&
-       (!reduce || (cudaMemset(L->acc, 0, static_cast<size_t>(L->Tmax) * H * 4) == cudaSuccess &&
-                    cudaMemset(L->acc_cnt, 0, static_cast<size_t>(L->Tmax) * (H / 128) * 4) ==
-                        cudaSuccess));
+       (!reduce || cudaMemset(L->acc, 0, static_cast<size_t>(L->Tmax) * H * 4) == cudaSuccess) &&
+       (!counted ||
+        cudaMemset(L->acc_cnt, 0, static_cast<size_t>(L->Tmax) * (H / 128) * 4) == cudaSuccess);
   for (int i = 0; i < 4 && ok; ++i) {
     ok = make_map(&L->maps1.a[i], L->xq, L->xb, Rpad, 16u << i) &&
          make_map(&L->maps2.a[i], L->hq, L->hb, Rpad, 16u << i);
@@ -519,7 +523,8 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   cudaError_t e;
   int launches = 4;
   const bool small = T <= kSmallFrontTokens;
-  if (small && L->single_launch && L->fused_gemms && L->combine == MOE_COMBINE_GATHER &&
+  // (the fused combine has the decode kernel's own combine for T <= 16)
+  if (small && L->single_launch && L->fused_gemms && L->combine != MOE_COMBINE_REDUCE &&
       (L->stage_scales || L->fmt == MOE_FMT_BF16)) {
     // the whole layer in one launch (timed as GEMM1)
     GemmArgs a1 = gemm1_args(L, 1, false);
@@ -580,7 +585,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   const int64_t chunks = max_chunks(L, T);
   const int pair = L->pair_scale_copies && T <= kPairCopyMaxTokens;
   const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && T > kPairCopyMaxTokens);
-  void* reduce_out = L->combine == MOE_COMBINE_REDUCE ? out : nullptr;
+  void* reduce_out = L->combine != MOE_COMBINE_GATHER ? out : nullptr;
   // decode: both GEMMs in one launch (for larger T the split measured faster)
   if (small && !wide && L->fused_gemms) {
     // one launch for both GEMMs (timed as GEMM1)

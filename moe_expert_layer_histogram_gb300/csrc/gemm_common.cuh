@@ -348,6 +348,57 @@ __device__ __forceinline__ void reduce_finish(int64_t t, int n_tile, const GemmA
   *cnt = 0;
 }
 
+// GEMM2 with the fused combine (a.gather_inv != nullptr), after the warp's
+// rows of a 128-column group have been stored: each stored row counts itself
+// for its token's group; for every token whose K-th row this warp stored,
+// the whole warp sums that token's K rows of the group in k order in fp32
+// (the combine kernel's operations, so the output is bit-identical), writes
+// the bf16 result and resets the counter for the next forward.  Called by
+// all 32 lanes of the warp; `stored`: this lane's row was stored.
+__device__ __forceinline__ void combine_fused(bool stored, int64_t prow, int n_tile,
+                                              const GemmArgs& a) {
+  constexpr unsigned kAll = 0xFFFFFFFFu;
+  const int lane = threadIdx.x & 31;
+  __threadfence();  // this lane's row is visible before it is counted
+  int t = 0;
+  bool last = false;
+  if (stored) {
+    t = a.prow_slot[prow] / a.K;
+    last = atomicAdd(a.acc_cnt + static_cast<int64_t>(t) * (a.H / 128) + n_tile, 1) == a.K - 1;
+  }
+  unsigned todo = __ballot_sync(kAll, last);
+  if (!todo) return;
+  __threadfence();  // the token's other rows, counted before, are visible
+  while (todo) {
+    const int src = __ffs(todo) - 1;
+    todo &= todo - 1;
+    const int64_t tt = __shfl_sync(kAll, t, src);
+    // lane l: columns 4l .. 4l+3 of the group
+    uint2 u[kMaxTopK];
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k)
+      if (k < a.K) {
+        const int64_t row = a.gather_inv[tt * a.K + k];
+        u[k] = __ldcg(reinterpret_cast<const uint2*>(a.out + row * a.out_ld + n_tile * 256) + lane);
+      }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k)
+      if (k < a.K) {
+        const float wk = a.topk_w[tt * a.K + k];
+        const float2 p0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[k].x));
+        const float2 p1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[k].y));
+        acc[0] = fmaf(wk, p0.x, acc[0]);
+        acc[1] = fmaf(wk, p0.y, acc[1]);
+        acc[2] = fmaf(wk, p1.x, acc[2]);
+        acc[3] = fmaf(wk, p1.y, acc[3]);
+      }
+    reinterpret_cast<uint2*>(a.comb_out + (tt * a.H + n_tile * 128) * 2)[lane] =
+        make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+    if (lane == src) a.acc_cnt[tt * (a.H / 128) + n_tile] = 0;
+  }
+}
+
 template <int FMT, int EPI>
 __device__ __forceinline__ void epilogue_round(const uint32_t* v, int p, bool store, int64_t prow,
                                                int64_t orow, int n_tile, const GemmArgs& a,

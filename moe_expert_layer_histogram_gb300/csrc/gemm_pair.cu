@@ -469,6 +469,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         uint32_t carry[5];
         epilogue_round<FMT, EPI>(v, 0, r < it.rows, prow, orow, n128, args, carry);
         epilogue_round<FMT, EPI>(v + 64, 1, r < it.rows, prow, orow, n128, args, carry);
+        if (EPI == 2 && args.gather_inv) combine_fused(r < it.rows, prow, n128, args);
       }
     }
   }

@@ -56,6 +56,11 @@ struct GemmArgs {
   const int32_t* prow_slot;  // padded row -> slot t*K + k
   const float* topk_w;       // [T*K]
   uint8_t* comb_out;         // bf16 [T, H]
+  // GEMM2 with the fused combine (gather_inv != nullptr): the K-th stored row
+  // of a token's 128-column group gathers the token's K rows of y (slot ->
+  // padded row) and writes the group of comb_out; acc_cnt counts the rows,
+  // prow_slot / topk_w as above, acc unused.
+  const int32_t* gather_inv;
   int K, H;
   int32_t* done1;            // fused GEMM1+GEMM2 launch: per expert, GEMM1 epilogue warps done
   int test_stall;            // test hook: CTA 0 never loads one stage, so the waits on it

@@ -524,3 +524,31 @@ def test_forward_on_a_side_stream():
     assert torch.equal(out, ref)
     assert layer.status() == 0
     layer.close()
+
+
+# ---- the combine fused into GEMM2's epilogue ---------------------------------
+@pytest.mark.parametrize("name,over,env", [
+    ("bf16_small", dict(), {}),                                           # narrow items
+    ("nvfp4_zipf_small", dict(T=1100, E=24, K=4), {}),                    # wide items
+    ("nvfp4_zipf_small", dict(T=1100, E=24, K=4), {"MOE_PAIR_CTAS": "1"}),  # CTA pairs
+    ("mxfp8_small", dict(act="relu2"), {}),
+    ("nvfp4_small", dict(T=12, E=40, K=8), {}),                            # single-launch decode
+    ("nvfp4_small", dict(T=12, E=40, K=8), {"MOE_SINGLE_LAUNCH": "0"}),    # fused decode GEMMs
+    ("nvfp4_small", dict(T=300, E=40, K=16), {}),                          # top-16
+], ids=["bf16", "nvfp4-wide", "nvfp4-pairs", "mxfp8-relu2", "decode", "decode-3-launch", "top16"])
+def test_fused_combine_is_bit_identical_to_the_combine_kernel(name, over, env, monkeypatch):
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    s = workloads.spec(name, **over)
+    case = workloads.make_case(s, seed=107)
+    ref = run_oracle(s, case)
+    outs = {}
+    for mode in ("gather", "fused"):
+        layer = make_layer(dict(s, combine=mode), weights=case["weights"])
+        got = [run_gpu(layer, case["hidden"], case["logits"]).cpu() for _ in range(2)]
+        assert layer.status() == 0
+        assert torch.equal(got[0], got[1])          # the counters are back at zero
+        outs[mode] = got[0]
+        layer.close()
+    assert torch.equal(outs["gather"], outs["fused"])
+    assert rel_l2(outs["fused"].float().numpy(), bf16_bits_to_f64(ref["out"])) <= TOL[s["fmt"]]
