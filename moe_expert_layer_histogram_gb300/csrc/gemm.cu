@@ -22,8 +22,16 @@
 // never stored.  Warp 1 (one thread) owns TMEM: it copies the scale tiles
 // into TMEM (tcgen05.cp) and issues 128 x (128 NW) tcgen05.mma into an fp32
 // accumulator (two of 128 columns, or one of 256 for wide items).  For decode
-// chunks warp 0 writes the scales with tcgen05.st instead, and for wide
-// NVFP4 GEMM1 items four stager warps (12-15, one per TMEM lane quarter) do.
+// chunks warp 0 writes the scales with tcgen05.st instead.  Wide NVFP4 items
+// keep their scale tiles in a ring of their own that warp 3 fills ahead of
+// the operands; four stager warps (12-15, one per TMEM lane quarter) write a
+// stage's scales into TMEM as soon as the stage's previous MMAs are done and
+// report on the stage's full barrier, so the MMA thread waits once per stage
+// and the staging overlaps the operand copies.  At N = 256 every K slice
+// moves about 127 KB through an SM's shared memory (54 KB of copies, 48 KB
+// of MMA operand reads, the stagers' scale reads): at 128 bytes per clock
+// that is about 490 ns, which is what a slice takes (measured 486 ns).  The
+// tensor pipe alone would take 262 ns.
 // The epilogue warps (3.., or 4-11 in the 16-warp wide NVFP4 kernel) drain
 // the accumulator (tcgen05.ld), run the epilogue and store, each thread one
 // row, in whole 32-byte sectors and marked L2 evict-first.  The token tile is the
@@ -52,6 +60,15 @@ __host__ __device__ constexpr int gemm_threads(int fmt, int nw) {
   return wide_stager(fmt, nw) ? 512 : 96 + 128 * nw;
 }
 
+// Dynamic shared memory of a kernel instance: the wide NVFP4 kernel adds the
+// scale ring's barriers (its slots take the bytes the stages no longer hold).
+template <int FMT, int MROWS, int NW>
+__host__ __device__ constexpr int gemm_smem() {
+  return smem_bytes<FMT, MROWS, NW>() +
+         (wide_stager(FMT, NW) ? 2 * num_stages<FMT, MROWS, NW>() * 8 : 0);
+}
+static_assert(gemm_smem<kFmtNVFP4, 128, 2>() <= kSmemLimit, "wide NVFP4 shared memory");
+
 // ---------------------------------------------------------------- kernel
 // FUSED (decode): one launch runs GEMM1's items (args/maps) and then
 // GEMM2's (args2/maps2).  Each CTA finishes issuing its GEMM1 items before
@@ -73,18 +90,29 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
   constexpr int kSfColsPerStage = Wide<NW>::kSfCols;
   constexpr bool WS = wide_stager(FMT, NW);
   constexpr int kEpiWarp0 = WS ? 4 : 3;  // first epilogue warp
-  // shared-memory offsets inside a stage
-  constexpr int kOffBsf = A_BYTES + NW * kTileBytes;        // weight scale tiles
-  constexpr int kOffAsf = kOffBsf + NW * SFT * 512;          // activation scale tiles
+  // Shared-memory offsets inside a stage (A codes, B codes, B scale tiles,
+  // A scale tiles).  Wide NVFP4 kernels keep the scale tiles in a ring of
+  // their own (SBO: operand stage bytes; the scale ring follows the operand
+  // stages, one slot per stage, the same bytes in total), filled ahead of
+  // the operands by warp 3, so that writing a stage's scales into TMEM is
+  // done by the time its operands land.
+  constexpr int SBO = WS ? A_BYTES + NW * kTileBytes : SB;
+  constexpr int kOffBsf = WS ? 0 : A_BYTES + NW * kTileBytes;  // weight scale tiles
+  constexpr int kOffAsf = kOffBsf + NW * SFT * 512;              // activation scale tiles
+  constexpr int kSfSlot = (NW + 1) * SFT * 512;                  // scale ring slot (WS)
+  static_assert(!WS || SBO + kSfSlot == SB, "wide stage layout");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sring = smem + kStages * SBO;  // WS: scale ring
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * SB);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drained = tempty + 2;
   uint64_t* sf_ready = drained + 1;  // [kStages] scales of the stage are in TMEM
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sf_ready + kStages);
+  uint64_t* sfull = sf_ready + kStages;   // WS: [kStages] scale ring slot landed
+  uint64_t* sempty = sfull + kStages;     // WS: [kStages] scale ring slot read
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sf_ready + kStages + (WS ? 2 * kStages : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_tab = reinterpret_cast<int*>(tmem_holder + 4);
   const Tables tab{s_tab, s_tab + (args.E + 1), s_tab + (2 * args.E + 1)};
@@ -93,9 +121,15 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      // WS with stagers: the stage's operand bytes and the four stager
+      // warps' reports that its scales are in TMEM
+      mbar_init(&full[s], WS && args.stage_scales ? 5 : 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_ready[s], WS ? 4 : 1);
+      mbar_init(&sf_ready[s], 1);
+      if constexpr (WS) {
+        mbar_init(&sfull[s], 1);
+        mbar_init(&sempty[s], args.stage_scales ? 4 : 1);
+      }
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -141,11 +175,10 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
   // quarters with tcgen05.st (the activation scales of quarter q in one
   // column per 64-element substep, the weight scales replicated in every
   // quarter) instead of the MMA thread broadcasting twelve tiles with
-  // tcgen05.cp; the copies queue in order with the MMAs on the tensor pipe.
-  // GEMM2 keeps the copies: its short items mostly stream weights from HBM,
-  // and the stagers' hop between a stage landing and its MMAs holds ring
-  // slots longer, which costs more bandwidth than the copies cost MMA time.
-  const bool wstaged = WS && EPI != 2 && args.stage_scales;
+  // tcgen05.cp, which queue in order with the MMAs on the tensor pipe
+  // (measured: twelve copies per K slice take a 128 x 256 x 256 slice from
+  // 262 to 483 ns of tensor-pipe time; staged scales leave it at the MMAs').
+  const bool wstaged = WS && args.stage_scales;
 
   // Roles by warpgroup: a warpgroup's register budget changes at the top of
   // its branch, before any of its roles' code.
@@ -245,7 +278,9 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
           }
           const uint64_t policy =
               tab.chunk_off[it.e + 1] - tab.chunk_off[it.e] > 1 ? reused : once;
-          const uint32_t bytes = (16u << amap) * 128u + NW * A.b_tile_bytes + SFT * 512u;
+          // WS: operand codes only (the scale ring carries the scale tiles)
+          const uint32_t bytes = WS ? (16u << amap) * 128u + NW * kTileBytes
+                                    : (16u << amap) * 128u + NW * A.b_tile_bytes + SFT * 512u;
           const uint8_t* sfa = A.sfa + static_cast<int64_t>(it.prow0 >> 7) * A.sfa_tiles_k * 512;
           // the item's first 128-row weight tile; the next one (NW = 2)
           // follows num_kb tiles later
@@ -266,7 +301,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
               }
               continue;
             }
-            uint8_t* sp = smem + stage * SB;
+            uint8_t* sp = smem + stage * SBO;
             mbar_arrive_expect_tx(&full[stage], bytes);
             tma_load_2d(sp, &amaps[amap], &full[stage], kb * 128, it.prow0);
             if constexpr (NW == 1) {
@@ -282,12 +317,12 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
                     btile + (static_cast<int64_t>(w) * A.num_kb + kb) * A.b_tile_bytes;
                 bulk_load_hint(sp + A_BYTES + w * kTileBytes, src, kTileBytes, &full[stage],
                                policy);
-                if constexpr (SFT > 0)
+                if constexpr (SFT > 0 && !WS)
                   bulk_load_hint(sp + kOffBsf + w * SFT * 512, src + kTileBytes, SFT * 512,
                                  &full[stage], policy);
               }
             }
-            if constexpr (SFT > 0)
+            if constexpr (SFT > 0 && !WS)
               bulk_load(sp + kOffAsf, sfa + kb * SFT * 512, SFT * 512, &full[stage]);
             ++slots;
             if (++stage == kStages) {
@@ -302,6 +337,56 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
           const int idx = slots - back;
           if (idx == skipped) continue;
           mbar_wait(&full[idx % kStages], static_cast<uint32_t>((idx / kStages) & 1), nullptr);
+        }
+        if (!ok) report_status(args.status, kStatusTimeout);
+      }
+    } else if (WS && warp == 3) {
+      // ------------------------------------------------ scale producer
+      // Fills the scale ring (both weight tiles' scale tiles and the
+      // activation scale tiles of each K slice) as far ahead of the operand
+      // ring as its slots allow; a slot is released once its scales are in
+      // TMEM (or, without the stagers, once the MMA thread's copies of them
+      // have completed).
+      if (lane == 0) {
+        const uint64_t once = l2_policy_evict_first();
+        const uint64_t reused = l2_policy_evict_normal();
+        int stage = 0;
+        uint32_t phase = 0;
+        int slots = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+          const GemmArgs& A = gargs(item);
+          const Item it = map_item(tab, args.E, A.n_tiles, local_item(item));
+          const uint64_t policy =
+              tab.chunk_off[it.e + 1] - tab.chunk_off[it.e] > 1 ? reused : once;
+          const uint8_t* sfa = A.sfa + static_cast<int64_t>(it.prow0 >> 7) * A.sfa_tiles_k * 512;
+          const uint8_t* btile =
+              A.b_tiles + (static_cast<int64_t>(it.e) * A.n_tiles + it.n_tile) * NW * A.num_kb *
+                              A.b_tile_bytes;
+          for (int kb = 0; kb < A.num_kb; ++kb) {
+            if (!mbar_wait(&sempty[stage], phase ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sp = sring + stage * kSfSlot;
+            mbar_arrive_expect_tx(&sfull[stage], kSfSlot);
+#pragma unroll
+            for (int w = 0; w < NW; ++w)
+              bulk_load_hint(sp + w * SFT * 512,
+                             btile + (static_cast<int64_t>(w) * A.num_kb + kb) * A.b_tile_bytes +
+                                 kTileBytes,
+                             SFT * 512, &sfull[stage], policy);
+            bulk_load(sp + kOffAsf, sfa + kb * SFT * 512, SFT * 512, &sfull[stage]);
+            ++slots;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        for (int back = 1; back <= kStages && back <= slots; ++back) {
+          const int idx = slots - back;
+          mbar_wait(&sfull[idx % kStages], static_cast<uint32_t>((idx / kStages) & 1), nullptr);
         }
         if (!ok) report_status(args.status, kStatusTimeout);
       }
@@ -336,15 +421,18 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem + buf * kAccCols;
           for (int kb = 0; kb < A.num_kb; ++kb) {
-            if (!mbar_wait(staged || wstaged ? &sf_ready[stage] : &full[stage], phase,
-                           abort_flag)) {
+            // (WS: full also counts the stagers' reports; without the
+            // stagers the scale ring slot is waited for separately)
+            if (!mbar_wait(staged ? &sf_ready[stage] : &full[stage], phase, abort_flag) ||
+                (WS && !wstaged && !mbar_wait(&sfull[stage], phase, abort_flag))) {
               ok = false;
               break;
             }
             tc_fence_after();
-            uint8_t* sp = smem + stage * SB;
+            uint8_t* sp = smem + stage * SBO;
             const uint32_t a_addr = smem_u32(sp), b_addr = smem_u32(sp + A_BYTES);
-            uint8_t* sf = sp + kOffBsf;  // weight scales, then activation scales
+            uint8_t* sfbase = WS ? sring + stage * kSfSlot : sp;
+            uint8_t* sf = sfbase + kOffBsf;  // weight scales, then activation scales
             const uint32_t sf_col = tmem + kSfColBase + stage * kSfColsPerStage;
             if constexpr (FMT == kFmtNVFP4 && NW == 2) {
               if (wstaged) {
@@ -356,7 +444,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
               } else {
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                tc_copy_sf(sf_col + j * 16, desc_sf(smem_u32(sp + kOffAsf + j * 512)));
+                tc_copy_sf(sf_col + j * 16, desc_sf(smem_u32(sfbase + kOffAsf + j * 512)));
                 tc_copy_sf(sf_col + j * 16 + 8, desc_sf(smem_u32(sf + j * 512)));
                 tc_copy_sf(sf_col + j * 16 + 12, desc_sf(smem_u32(sf + (SFT + j) * 512)));
               }
@@ -368,7 +456,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
             } else if constexpr (FMT == kFmtMXFP8 && NW == 2) {
               tc_copy_sf(sf_col, desc_sf(smem_u32(sf)));
               tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf + 512)));
-              tc_copy_sf(sf_col + 8, desc_sf(smem_u32(sp + kOffAsf)));
+              tc_copy_sf(sf_col + 8, desc_sf(smem_u32(sfbase + kOffAsf)));
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 mma_mxf8(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32),
@@ -425,6 +513,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
                          (kb | j) != 0);
             }
             tc_commit(&empty[stage]);
+            if (WS && !wstaged) tc_commit(&sempty[stage]);  // its scale copies are done
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -444,7 +533,11 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
       // columns 8j..8j+7 (row n at column 8j + n/32, lane n % 32: every quarter
       // holds all of them), and its own 32 activation rows' scales in column
       // 32 + 4j + q (the MMA of quarter q reads column q of the four starting
-      // at the activation scale address).
+      // at the activation scale address).  A stage's columns are free once
+      // the MMAs of the stage's previous use have completed (its empty
+      // barrier), its scales come from the scale ring, and the report goes
+      // to the stage's full barrier, which the MMA thread waits on anyway:
+      // the scales are staged while the operands are still in flight.
       if (wstaged) {
         const int q = warp & 3;
         int stage = 0;
@@ -453,12 +546,14 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
         for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
           const GemmArgs& A = gargs(item);
           for (int kb = 0; kb < A.num_kb; ++kb) {
-            const bool landed = mbar_wait(&full[stage], phase, abort_flag);
-            if (!__all_sync(0xFFFFFFFFu, landed)) {
+            const bool ready = mbar_wait(&sfull[stage], phase, abort_flag) &&
+                               mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, ready)) {
               ok = false;
               break;
             }
-            const uint8_t* sp = smem + stage * SB;
+            tc_fence_after();
+            const uint8_t* sp = sring + stage * kSfSlot;
             uint32_t v[32];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -474,17 +569,24 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
               v[8 * j + 6] = b1.z;
               v[8 * j + 7] = b1.w;
             }
+            uint32_t a4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              a4[j] = *reinterpret_cast<const uint32_t*>(sp + kOffAsf + j * 512 + lane * 16 + q * 4);
+            // the ring slot has been read; the next bulk copy into it is an
+            // async-proxy write after these generic-proxy reads
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sempty[stage]);
             const uint32_t col = tmem + (static_cast<uint32_t>(q * 32) << 16) + kSfColBase +
                                  stage * kSfColsPerStage;
             tmem_st32(col, v);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tmem_st1(col + 32 + 4 * j + q, *reinterpret_cast<const uint32_t*>(
-                                                 sp + kOffAsf + j * 512 + lane * 16 + q * 4));
+            for (int j = 0; j < 4; ++j) tmem_st1(col + 32 + 4 * j + q, a4[j]);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sf_ready[stage]);
+            if (lane == 0) mbar_arrive(&full[stage]);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -591,7 +693,7 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, const GemmMap
   if (wide_stager(FMT, NW) && !split_checked<FMT, EPI, MROWS, NW, FUSED>())
     return cudaErrorInvalidConfiguration;
   return launch_pdl(g_pdl_gemm, moe_gemm_kernel<FMT, EPI, MROWS, NW, FUSED>, dim3(grid),
-                    dim3(gemm_threads(FMT, NW)), smem_bytes<FMT, MROWS, NW>(), s, maps, args,
+                    dim3(gemm_threads(FMT, NW)), gemm_smem<FMT, MROWS, NW>(), s, maps, args,
                     maps2, args2);
 }
 
@@ -599,7 +701,7 @@ template <int FMT, int EPI, int MROWS, int NW, bool FUSED = false>
 cudaError_t set_smem() {
   cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<FMT, EPI, MROWS, NW, FUSED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes<FMT, MROWS, NW>());
+                                       gemm_smem<FMT, MROWS, NW>());
   if (e != cudaSuccess || !wide_stager(FMT, NW)) return e;
   // The kernel's register split only balances at kSplitLaunchRegs registers
   // per thread; with fewer, the claiming warpgroups would wait forever.
