@@ -23,8 +23,8 @@
 
 using namespace moe;
 
-bool moe::g_pdl_small = true;
-bool moe::g_pdl_gemm = true;
+thread_local bool moe::g_pdl_small = true;
+thread_local bool moe::g_pdl_gemm = true;
 
 struct moe_layer {
   moe_config cfg;
@@ -62,6 +62,9 @@ struct moe_layer {
   int test_stall = 0;                // fault injection (moe_config.test_stall_gemm): GEMM1 times out
   int max_ctas = 0;                  // CTAs per GEMM launch (moe_config.max_ctas, else the SM count)
   int pair_clusters = 0;             // NVFP4 wide launches: co-resident CTA pairs (0: single CTAs)
+  bool pdl_small = true;             // programmatic dependent launch of the small kernels
+  bool pdl_gemm = true;              // ... of the GEMM kernels
+  bool pdl_prefill = false;          // ... also for prefill-sized (wide) forwards
   bool weights_ready = false;
   int last_T = 0, last_launches = 0;
   std::vector<cudaEvent_t> tev;  // per-kernel timing events, 7 per forward
@@ -156,6 +159,15 @@ constexpr int kPairCopyMaxTokens = 1024;
 int64_t max_chunks(const moe_layer* L, int T) {
   const int64_t R = static_cast<int64_t>(T) * L->K;
   return std::min<int64_t>(L->E, R) + R / kRowBlock;
+}
+
+// Launch attributes of this forward's kernels (read by launch_pdl on this
+// host thread): programmatic dependent launch for decode-sized forwards,
+// plain stream order for wide (prefill) ones unless MOE_PDL_PREFILL=1.
+void set_pdl(const moe_layer* L, bool wide) {
+  const bool on = !wide || L->pdl_prefill;
+  g_pdl_small = L->pdl_small && on;
+  g_pdl_gemm = L->pdl_gemm && on;
 }
 
 // GEMM1 (+ the activation and re-quantisation) over the padded
@@ -338,17 +350,19 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
     return MOE_ERR_NO_DEVICE;
   }
   if (!encode_fn()) return MOE_ERR_NO_DEVICE;
-  {
-    const char* v = std::getenv("MOE_DISABLE_PDL");
-    const std::string off = v ? v : "";
-    g_pdl_small = !(off == "1" || off == "small");
-    g_pdl_gemm = !(off == "1" || off == "gemm");
-  }
   const char* pv = std::getenv("MOE_PAIR_SCALE_COPIES");
 
   moe_layer* L = new moe_layer;
   L->cfg = c;
   L->device = dev;
+  {
+    const char* v = std::getenv("MOE_DISABLE_PDL");
+    const std::string off = v ? v : "";
+    L->pdl_small = !(off == "1" || off == "small");
+    L->pdl_gemm = !(off == "1" || off == "gemm");
+    const char* pp = std::getenv("MOE_PDL_PREFILL");
+    L->pdl_prefill = pp && pp[0] == '1';
+  }
   L->num_sms = sms;
   L->fmt = c.format;
   L->H = c.hidden;
@@ -523,6 +537,8 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   cudaError_t e;
   int launches = 4;
   const bool small = T <= kSmallFrontTokens;
+  const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && T > kPairCopyMaxTokens);
+  set_pdl(L, wide);
   // (the fused combine has the decode kernel's own combine for T <= 16)
   if (small && L->single_launch && L->fused_gemms && L->combine != MOE_COMBINE_REDUCE &&
       (L->stage_scales || L->fmt == MOE_FMT_BF16)) {
@@ -584,7 +600,6 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   mark(3);
   const int64_t chunks = max_chunks(L, T);
   const int pair = L->pair_scale_copies && T <= kPairCopyMaxTokens;
-  const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && T > kPairCopyMaxTokens);
   void* reduce_out = L->combine != MOE_COMBINE_GATHER ? out : nullptr;
   // decode: both GEMMs in one launch (for larger T the split measured faster)
   if (small && !wide && L->fused_gemms) {
@@ -622,10 +637,11 @@ moe_status moe_forward_batched(moe_layer* L, const void* hidden, const int32_t* 
   const int64_t chunks = mpad / kRowBlock * L->E;
   // every chunk holds at most 32 rows when M <= 32: the lanes-0-31 scale copies apply
   const int pair = L->pair_scale_copies && M <= 32;
+  const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && M >= 256);
+  set_pdl(L, wide);
   cudaError_t e = launch_batched_quant(L->fmt, hidden, counts, M, L->E, L->H, L->counts,
                                        L->offsets, L->pad_off, L->chunk_off, L->xq, L->xsf,
                                        L->status, s);
-  const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && M >= 256);
   if (e == cudaSuccess) e = run_gemm1(L, chunks, M, pair, wide, s);
   if (e == cudaSuccess) e = run_gemm2(L, chunks, M, pair, wide, out, M, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;

@@ -420,9 +420,44 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem + buf * kAccCols;
+          if constexpr (WS) {
+            if (wstaged) {
+              // The wide NVFP4 main loop, kept short: this thread's own time
+              // per K slice (the wait, four MMA issues, the commit, the loop)
+              // must stay below the tensor pipe's 262 ns for the pipe to stay
+              // busy.  Descriptors advance by adding 16-byte units to the
+              // start-address field (shared memory stays below 256 KiB, so
+              // the field never carries).
+              const uint64_t da0 = desc_sw128(smem_u32(smem));
+              const uint32_t sf0 = tmem + kSfColBase;
+              const int nkb = A.num_kb;
+              for (int kb = 0; kb < nkb; ++kb) {
+                // full counts the operand bytes and the stagers' reports
+                if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint64_t da = da0 + static_cast<uint64_t>(stage * (SBO >> 4));
+                const uint64_t db = da + (A_BYTES >> 4);
+                const uint32_t sfc = sf0 + stage * kSfColsPerStage;
+                mma_nvf4(d_tmem, da, db, idesc, sfc + 32, sfc, kb != 0);
+                mma_nvf4(d_tmem, da + 2, db + 2, idesc, sfc + 36, sfc + 8, 1u);
+                mma_nvf4(d_tmem, da + 4, db + 4, idesc, sfc + 40, sfc + 16, 1u);
+                mma_nvf4(d_tmem, da + 6, db + 6, idesc, sfc + 44, sfc + 24, 1u);
+                tc_commit(&empty[stage]);
+                if (++stage == kStages) {
+                  stage = 0;
+                  phase ^= 1u;
+                }
+              }
+              if (ok) tc_commit(&tfull[buf]);
+              continue;
+            }
+          }
           for (int kb = 0; kb < A.num_kb; ++kb) {
-            // (WS: full also counts the stagers' reports; without the
-            // stagers the scale ring slot is waited for separately)
+            // (WS without the stagers: the scale ring slot is waited for
+            // separately)
             if (!mbar_wait(staged ? &sf_ready[stage] : &full[stage], phase, abort_flag) ||
                 (WS && !wstaged && !mbar_wait(&sfull[stage], phase, abort_flag))) {
               ok = false;
@@ -435,13 +470,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
             uint8_t* sf = sfbase + kOffBsf;  // weight scales, then activation scales
             const uint32_t sf_col = tmem + kSfColBase + stage * kSfColsPerStage;
             if constexpr (FMT == kFmtNVFP4 && NW == 2) {
-              if (wstaged) {
-                // the stager warps wrote this stage's scale columns
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
-                           sf_col + 32 + j * 4, sf_col + j * 8, (kb | j) != 0);
-              } else {
+              // without the stagers: the MMA thread copies the scale tiles
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 tc_copy_sf(sf_col + j * 16, desc_sf(smem_u32(sfbase + kOffAsf + j * 512)));
@@ -452,7 +481,6 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
               for (int j = 0; j < 4; ++j)
                 mma_nvf4(d_tmem, desc_sw128(a_addr + j * 32), desc_sw128(b_addr + j * 32), idesc,
                          sf_col + j * 16, sf_col + j * 16 + 8, (kb | j) != 0);
-              }
             } else if constexpr (FMT == kFmtMXFP8 && NW == 2) {
               tc_copy_sf(sf_col, desc_sf(smem_u32(sf)));
               tc_copy_sf(sf_col + 4, desc_sf(smem_u32(sf + 512)));

@@ -87,14 +87,16 @@ struct GemmMaps {
 constexpr int weight_sf_tiles(int fmt) { return fmt == kFmtNVFP4 ? 4 : fmt == kFmtMXFP8 ? 1 : 0; }
 constexpr int weight_tile_bytes(int fmt) { return 128 * 128 + 512 * weight_sf_tiles(fmt); }
 
-// Programmatic dependent launch: every kernel of the forward is launched
-// with programmatic stream serialization, lets its dependents launch as soon
-// as it starts, runs its input-independent prologue and waits for the
-// previous kernel (griddepcontrol.wait) before it touches data that kernel
-// produced or still reads.  It can be switched off for comparison, read at
-// moe_create: MOE_DISABLE_PDL=1 (all kernels), =gemm (the two GEMMs),
-// =small (the others).
-extern bool g_pdl_small, g_pdl_gemm;
+// Programmatic dependent launch: every kernel of a decode-sized forward is
+// launched with programmatic stream serialization, lets its dependents
+// launch as soon as it starts, runs its input-independent prologue and
+// waits for the previous kernel (griddepcontrol.wait) before it touches data
+// that kernel produced or still reads.  Prefill-sized (wide) forwards launch
+// without it: there the early dependents measured slower (T = 32768: 7.26 ->
+// 6.38 ms per layer without; T = 8192: 1.94 -> 1.88 ms).  Set per forward on
+// the calling host thread from the layer's settings (moe_create reads
+// MOE_DISABLE_PDL=1|gemm|small and MOE_PDL_PREFILL=1).
+extern thread_local bool g_pdl_small, g_pdl_gemm;
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
