@@ -86,9 +86,11 @@ typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_RELU2 = 1 } moe_activation;
  * stored sums the token's K rows in k order in fp32 and writes the bf16
  * result (bit-identical to GATHER), so no combine kernel runs (the combine
  * folded into the expert GEMM, as the MegaMoE kernel fuses its FC2 with the
- * reduction, sec. 六; here without atomics on the output).  Measured slower
- * than GATHER on GB300 for T > 16 (the gathers lengthen GEMM2's epilogue);
- * for T <= 16 the single-launch decode kernel's own combine is used.     */
+ * reduction, sec. 六; here without atomics on the output).  Only
+ * prefill-sized launches (T > 1024, the 256-column GEMM items) fuse it;
+ * smaller ones run the combine kernel (T <= 16: the single-launch decode
+ * kernel's own combine), so their GEMM kernels carry no gather.  Measured
+ * slower than GATHER on GB300 (the gathers lengthen GEMM2's epilogue).     */
 typedef enum {
     MOE_COMBINE_GATHER = 0,
     MOE_COMBINE_REDUCE = 1,

@@ -600,7 +600,10 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   mark(3);
   const int64_t chunks = max_chunks(L, T);
   const int pair = L->pair_scale_copies && T <= kPairCopyMaxTokens;
-  void* reduce_out = L->combine != MOE_COMBINE_GATHER ? out : nullptr;
+  // the fused combine runs in wide (prefill) GEMM2 launches only; narrower
+  // launches keep the combine kernel (their GEMM2 kernels carry no gather)
+  const bool fused_combine = L->combine == MOE_COMBINE_FUSED && wide;
+  void* reduce_out = L->combine == MOE_COMBINE_REDUCE || fused_combine ? out : nullptr;
   // decode: both GEMMs in one launch (for larger T the split measured faster)
   if (small && !wide && L->fused_gemms) {
     // one launch for both GEMMs (timed as GEMM1)
@@ -613,8 +616,8 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, wide, L->y, 0, s, out);
   }
   mark(5);
-  // with the in-kernel reduce GEMM2 has written `out` already
-  if (e == cudaSuccess && L->combine == MOE_COMBINE_GATHER)
+  // with the in-kernel reduce or the fused combine GEMM2 has written `out` already
+  if (e == cudaSuccess && reduce_out == nullptr)
     e = launch_combine(L->y, L->inv, L->w, T, K, H, out, s);
   else
     --launches;

@@ -667,7 +667,6 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
             if (g2) epilogue_round<FMT, 2>(v, p, r < it.rows, prow, orow, n128, A, carry);
             else epilogue_round<FMT, EPI>(v, p, r < it.rows, prow, orow, n128, A, carry);
           }
-          if ((EPI == 2 || g2) && A.gather_inv) combine_fused(r < it.rows, prow, n128, A);
         }
         tc_fence_before();
         __syncwarp();

@@ -528,7 +528,7 @@ def test_forward_on_a_side_stream():
 
 # ---- the combine fused into GEMM2's epilogue ---------------------------------
 @pytest.mark.parametrize("name,over,env", [
-    ("bf16_small", dict(), {}),                                           # narrow items
+    ("bf16_small", dict(), {}),                                           # narrow: combine kernel
     ("nvfp4_zipf_small", dict(T=1100, E=24, K=4), {}),                    # wide items
     ("nvfp4_zipf_small", dict(T=1100, E=24, K=4), {"MOE_PAIR_CTAS": "1"}),  # CTA pairs
     ("mxfp8_small", dict(act="relu2"), {}),
