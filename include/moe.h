@@ -214,6 +214,23 @@ moe_status moe_forward_host(moe_layer *layer, const void *hidden_host,
                             const float *router_logits_host, void *out_host,
                             int T, void *stream);
 
+/* (The build's own call, no counterpart on the pages.)  moe_forward with
+ * HOST buffers, pipelined: enqueues the copy of hidden [T,H] bf16 and
+ * router_logits [T,E] f32 to the device, the layer, and the copy of out
+ * [T,H] bf16 back, and returns without waiting.  `stream` completes once
+ * out_host holds the result; until then the three host buffers must stay
+ * as they are (page-locked memory lets the copies overlap).  The copies run
+ * on a copy stream and the layer on a compute stream of the layer's own
+ * (created on the first call), both ordered after the work `stream` held at
+ * the call.  Consecutive calls overlap: step i+1's input copy waits only
+ * until step i's front end has read the device input buffers, and step i's
+ * output copy runs while step i+1 computes.  One layer's calls must come
+ * from one host thread at a time.  Errors as moe_forward; MOE_ERR_CUDA if
+ * the streams cannot be created.                                          */
+moe_status moe_forward_host_async(moe_layer *layer, const void *hidden_host,
+                                  const float *router_logits_host,
+                                  void *out_host, int T, void *stream);
+
 /* Inspection of the latest forward (tests; the build's own call, no
  * counterpart on the pages): device destinations, any may be NULL.  topk_ids int32 [T,K], topk_w f32 [T,K], offsets int32 [E+1]
  * (offsets[e] = first permuted row of expert e, offsets[E] = T*K),

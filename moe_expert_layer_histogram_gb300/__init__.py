@@ -41,7 +41,7 @@ class MoEError(RuntimeError):
 
 
 EXPORTS = ("moe_create", "moe_prepare_weights", "moe_forward", "moe_forward_batched",
-           "moe_forward_host",
+           "moe_forward_host", "moe_forward_host_async",
            "moe_debug_routing", "moe_debug_act_quant", "moe_debug_intermediates",
            "moe_debug_weight_tiles",
            "moe_get_status", "moe_timing_start", "moe_timing_stop", "moe_last_launch_count",
@@ -65,6 +65,7 @@ def lib():
     L.moe_prepare_weights.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_forward.argtypes = [vp, vp, vp, vp, ci, vp]
     L.moe_forward_host.argtypes = [vp, vp, vp, vp, ci, vp]
+    L.moe_forward_host_async.argtypes = [vp, vp, vp, vp, ci, vp]
     L.moe_forward_batched.argtypes = [vp, vp, vp, ci, vp, vp]
     L.moe_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp]
     L.moe_debug_act_quant.argtypes = [vp, vp, vp, vp]
@@ -138,6 +139,13 @@ def moe_forward_batched(handle, hidden, counts, M, out, stream=None):
 def moe_forward_host(handle, hidden_host, router_logits_host, out_host, T, stream=None):
     _check(lib().moe_forward_host(handle, _ptr(hidden_host), _ptr(router_logits_host),
                                   _ptr(out_host), int(T), stream), "moe_forward_host")
+
+
+def moe_forward_host_async(handle, hidden_host, router_logits_host, out_host, T, stream=None):
+    """Pipelined host-buffer forward: returns at once; `stream` completes
+    once out_host holds the result (keep the host buffers until then)."""
+    _check(lib().moe_forward_host_async(handle, _ptr(hidden_host), _ptr(router_logits_host),
+                                        _ptr(out_host), int(T), stream), "moe_forward_host_async")
 
 
 def moe_debug_routing(handle, topk_ids=None, topk_w=None, offsets=None, perm=None, stream=None):

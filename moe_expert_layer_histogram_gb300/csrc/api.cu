@@ -55,6 +55,13 @@ struct moe_layer {
   int* status = nullptr;
   uint8_t *h_in = nullptr, *o_out = nullptr;
   float* l_in = nullptr;
+  // moe_forward_host_async: streams for the input copies, the layer and the
+  // output copies, and their events (created on first use); ev_user marks
+  // the latest work on the layer enqueued on a caller's stream by the other
+  // entry points
+  cudaStream_t xi = nullptr, xo = nullptr, cs = nullptr;
+  cudaEvent_t ev_in = nullptr, ev_front = nullptr, ev_comb = nullptr, ev_d2h = nullptr,
+              ev_user = nullptr;
   GemmMaps maps1{}, maps2{};
   int pair_scale_copies = 1;
   int wide_tiles = -1;               // 0 off, 1 always, -1 for prefill-sized launches
@@ -159,6 +166,17 @@ constexpr int kPairCopyMaxTokens = 1024;
 int64_t max_chunks(const moe_layer* L, int T) {
   const int64_t R = static_cast<int64_t>(T) * L->K;
   return std::min<int64_t>(L->E, R) + R / kRowBlock;
+}
+
+// Work that another entry point enqueues on the caller's stream s is
+// ordered after the pipelined forwards' layer work (before_call), and the
+// next pipelined forward after it (after_call).  No-ops until
+// moe_forward_host_async has been used on the layer.
+void before_call(const moe_layer* L, cudaStream_t s) {
+  if (L->cs) cudaStreamWaitEvent(s, L->ev_comb, 0);
+}
+void after_call(const moe_layer* L, cudaStream_t s) {
+  if (L->cs) cudaEventRecord(L->ev_user, s);
 }
 
 // Launch attributes of this forward's kernels (read by launch_pdl on this
@@ -494,6 +512,7 @@ moe_status moe_prepare_weights(moe_layer* L, const void* w13, const void* w13_sf
   if (L->fmt != MOE_FMT_BF16 && (!w13_sf || !w2_sf)) return MOE_ERR_INVALID_ARG;
   if (L->fmt == MOE_FMT_NVFP4 && (!w13_gs || !w2_gs)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  before_call(L, s);
   const int E = L->E, H = L->H, I = L->I;
   cudaError_t e = launch_tile_weights(L->fmt, static_cast<const uint8_t*>(w13),
                                       static_cast<const uint8_t*>(w13_sf), w13_gs, L->w13t, E,
@@ -503,6 +522,7 @@ moe_status moe_prepare_weights(moe_layer* L, const void* w13, const void* w13_sf
     e = launch_tile_weights(L->fmt, static_cast<const uint8_t*>(w2),
                             static_cast<const uint8_t*>(w2_sf), w2_gs, L->w2t, E, H, L->hb,
                             L->h_tiles_k * 4, 0, s);
+  after_call(L, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   L->weights_ready = true;
   return MOE_OK;
@@ -515,17 +535,15 @@ bool io_aligned(const void* hidden, const void* logits, const void* out) {
          (reinterpret_cast<uintptr_t>(logits) & 3) == 0;
 }
 
-moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, void* out, int T,
-                       void* stream) {
-  if (!L || T < 0 || T > L->Tmax) return MOE_ERR_INVALID_ARG;
-  if (T == 0) {
-    L->last_T = 0;
-    L->last_launches = 0;
-    return MOE_OK;
-  }
-  if (!hidden || !logits || !out || !io_aligned(hidden, logits, out)) return MOE_ERR_INVALID_ARG;
-  if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+}  // extern "C"
+
+namespace {
+
+// The routed forward on stream s.  front_done (if any) is recorded once the
+// kernels that read `hidden` and `logits` have been enqueued; s waits for
+// before_out (if any) before the first kernel that writes `out`.
+moe_status forward_impl(moe_layer* L, const void* hidden, const float* logits, void* out, int T,
+                        cudaStream_t s, cudaEvent_t front_done, cudaEvent_t before_out) {
   const int E = L->E, K = L->K, H = L->H;
   const int NB = (T + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
   cudaEvent_t* ev = nullptr;
@@ -569,8 +587,10 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
     mark(1);
     mark(2);
     mark(3);
+    if (before_out) cudaStreamWaitEvent(s, before_out, 0);
     e = launch_decode(L->fmt, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a1, L->maps2, a2, d,
                       grid, s);
+    if (front_done) cudaEventRecord(front_done, s);
     mark(4);
     mark(5);
     mark(6);
@@ -597,6 +617,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
                                L->prow_slot, L->xq, L->xsf, s);
     launches = 6;
   }
+  if (front_done) cudaEventRecord(front_done, s);
   mark(3);
   const int64_t chunks = max_chunks(L, T);
   const int pair = L->pair_scale_copies && T <= kPairCopyMaxTokens;
@@ -605,6 +626,7 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   const bool fused_combine = L->combine == MOE_COMBINE_FUSED && wide;
   void* reduce_out = L->combine == MOE_COMBINE_REDUCE || fused_combine ? out : nullptr;
   // decode: both GEMMs in one launch (for larger T the split measured faster)
+  if (before_out && reduce_out) cudaStreamWaitEvent(s, before_out, 0);  // GEMM2 writes out
   if (small && !wide && L->fused_gemms) {
     // one launch for both GEMMs (timed as GEMM1)
     if (e == cudaSuccess) e = run_gemms_fused(L, chunks, T, pair, reduce_out, s);
@@ -617,8 +639,10 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   }
   mark(5);
   // with the in-kernel reduce or the fused combine GEMM2 has written `out` already
-  if (e == cudaSuccess && reduce_out == nullptr)
+  if (e == cudaSuccess && reduce_out == nullptr) {
+    if (before_out) cudaStreamWaitEvent(s, before_out, 0);
     e = launch_combine(L->y, L->inv, L->w, T, K, H, out, s);
+  }
   else
     --launches;
   mark(6);
@@ -626,6 +650,27 @@ moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, vo
   L->last_T = T;
   L->last_launches = launches;
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward(moe_layer* L, const void* hidden, const float* logits, void* out, int T,
+                       void* stream) {
+  if (!L || T < 0 || T > L->Tmax) return MOE_ERR_INVALID_ARG;
+  if (T == 0) {
+    L->last_T = 0;
+    L->last_launches = 0;
+    return MOE_OK;
+  }
+  if (!hidden || !logits || !out || !io_aligned(hidden, logits, out)) return MOE_ERR_INVALID_ARG;
+  if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  before_call(L, s);
+  const moe_status st = forward_impl(L, hidden, logits, out, T, s, nullptr, nullptr);
+  after_call(L, s);
+  return st;
 }
 
 moe_status moe_forward_batched(moe_layer* L, const void* hidden, const int32_t* counts, int M,
@@ -642,11 +687,13 @@ moe_status moe_forward_batched(moe_layer* L, const void* hidden, const int32_t* 
   const int pair = L->pair_scale_copies && M <= 32;
   const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && M >= 256);
   set_pdl(L, wide);
+  before_call(L, s);
   cudaError_t e = launch_batched_quant(L->fmt, hidden, counts, M, L->E, L->H, L->counts,
                                        L->offsets, L->pad_off, L->chunk_off, L->xq, L->xsf,
                                        L->status, s);
   if (e == cudaSuccess) e = run_gemm1(L, chunks, M, pair, wide, s);
   if (e == cudaSuccess) e = run_gemm2(L, chunks, M, pair, wide, out, M, s);
+  after_call(L, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   L->last_T = 0;
   L->last_launches = 3;
@@ -660,6 +707,12 @@ moe_status moe_forward_host(moe_layer* L, const void* hidden_host, const float* 
   if (!hidden_host || !logits_host || !out_host) return MOE_ERR_INVALID_ARG;
   if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // (synchronous: a pipeline of moe_forward_host_async steps on the layer
+  // finishes first, since this call reuses its device buffers)
+  if (L->cs && (cudaStreamSynchronize(L->xi) != cudaSuccess ||
+                cudaStreamSynchronize(L->cs) != cudaSuccess ||
+                cudaStreamSynchronize(L->xo) != cudaSuccess))
+    return MOE_ERR_CUDA;
   // Page-locked host buffers the device can address (on a Grace-Blackwell
   // node over NVLink-C2C) are read and written by the kernels in place: the
   // front end reads the hidden states and logits, the combine writes the
@@ -684,17 +737,64 @@ moe_status moe_forward_host(moe_layer* L, const void* hidden_host, const float* 
   return MOE_OK;
 }
 
+moe_status moe_forward_host_async(moe_layer* L, const void* hidden_host, const float* logits_host,
+                                  void* out_host, int T, void* stream) {
+  if (!L || T < 0 || T > L->Tmax) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return moe_forward(L, nullptr, nullptr, nullptr, 0, stream);
+  if (!hidden_host || !logits_host || !out_host) return MOE_ERR_INVALID_ARG;
+  if (!L->weights_ready) return MOE_ERR_NO_WEIGHTS;
+  if (!L->cs) {
+    bool ok = true;
+    for (cudaStream_t* x : {&L->xi, &L->xo, &L->cs})
+      ok = ok && cudaStreamCreateWithFlags(x, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t* e : {&L->ev_in, &L->ev_front, &L->ev_comb, &L->ev_d2h, &L->ev_user})
+      ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t hb = static_cast<size_t>(T) * L->H * 2, lb = static_cast<size_t>(T) * L->E * 4;
+  // The input copies wait until the previous step's front end has read
+  // h_in and l_in; the layer waits for them and for the latest work other
+  // entry points enqueued on the layer; its output kernel waits until the
+  // previous step's output copy has read o_out.  (Waiting on an event that
+  // was never recorded is a no-op.)
+  bool ok = cudaStreamWaitEvent(L->xi, L->ev_front, 0) == cudaSuccess &&
+            cudaMemcpyAsync(L->h_in, hidden_host, hb, cudaMemcpyHostToDevice, L->xi) ==
+                cudaSuccess &&
+            cudaMemcpyAsync(L->l_in, logits_host, lb, cudaMemcpyHostToDevice, L->xi) ==
+                cudaSuccess &&
+            cudaEventRecord(L->ev_in, L->xi) == cudaSuccess &&
+            cudaStreamWaitEvent(L->cs, L->ev_in, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(L->cs, L->ev_user, 0) == cudaSuccess;
+  if (!ok) return MOE_ERR_CUDA;
+  moe_status st = forward_impl(L, L->h_in, L->l_in, L->o_out, T, L->cs, L->ev_front, L->ev_d2h);
+  if (st != MOE_OK) return st;
+  // the caller's stream completes once out_host holds the result; nothing
+  // of the layer waits on the caller's stream, so consecutive steps overlap
+  ok = cudaEventRecord(L->ev_comb, L->cs) == cudaSuccess &&
+       cudaStreamWaitEvent(L->xo, L->ev_comb, 0) == cudaSuccess &&
+       cudaMemcpyAsync(out_host, L->o_out, hb, cudaMemcpyDeviceToHost, L->xo) == cudaSuccess &&
+       cudaEventRecord(L->ev_d2h, L->xo) == cudaSuccess &&
+       cudaStreamWaitEvent(s, L->ev_d2h, 0) == cudaSuccess;
+  return ok ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status moe_debug_routing(moe_layer* L, int32_t* topk_ids, float* topk_w, int32_t* offsets,
                              int32_t* perm, void* stream) {
   if (!L) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t R = static_cast<size_t>(L->last_T) * L->K;
+  before_call(L, s);
   bool ok = true;
   if (topk_ids && R) ok &= cudaMemcpyAsync(topk_ids, L->ids, R * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
   if (topk_w && R) ok &= cudaMemcpyAsync(topk_w, L->w, R * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
   if (offsets && R)
     ok &= cudaMemcpyAsync(offsets, L->offsets, (L->E + 1) * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
   if (perm && R) ok &= cudaMemcpyAsync(perm, L->perm, R * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  after_call(L, s);
   return ok ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -702,10 +802,12 @@ moe_status moe_debug_act_quant(moe_layer* L, uint8_t* codes, uint8_t* scales, vo
   if (!L || !codes || !scales) return MOE_ERR_INVALID_ARG;
   if (L->fmt == MOE_FMT_BF16) return MOE_ERR_UNSUPPORTED;
   if (L->last_T == 0) return MOE_OK;
-  return launch_debug_act(L->fmt, L->inv, L->last_T, L->K, L->H, L->xq, L->xsf, codes, scales,
-                          static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? MOE_OK
-             : MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  before_call(L, s);
+  const bool ok = launch_debug_act(L->fmt, L->inv, L->last_T, L->K, L->H, L->xq, L->xsf, codes,
+                                   scales, s) == cudaSuccess;
+  after_call(L, s);
+  return ok ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_debug_weight_tiles(moe_layer* L, int which, int expert, void* dst,
@@ -729,10 +831,12 @@ moe_status moe_debug_intermediates(moe_layer* L, float* h, float* y, void* strea
   if (!L) return MOE_ERR_INVALID_ARG;
   const int R = L->last_T * L->K;
   if (R == 0 || (!h && !y)) return MOE_OK;
-  return launch_debug_rows(L->fmt, L->offsets, L->pad_off, L->E, R, L->I, L->H, L->hq, L->hsf,
-                           L->y, h, y, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? MOE_OK
-             : MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  before_call(L, s);
+  const bool ok = launch_debug_rows(L->fmt, L->offsets, L->pad_off, L->E, R, L->I, L->H, L->hq,
+                                    L->hsf, L->y, h, y, s) == cudaSuccess;
+  after_call(L, s);
+  return ok ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_get_status(moe_layer* L) {
@@ -808,6 +912,10 @@ void moe_destroy(moe_layer* L) {
   if (!L) return;
   cudaDeviceSynchronize();
   for (cudaEvent_t e : L->tev) cudaEventDestroy(e);
+  for (cudaEvent_t e : {L->ev_in, L->ev_front, L->ev_comb, L->ev_d2h, L->ev_user})
+    if (e) cudaEventDestroy(e);
+  for (cudaStream_t x : {L->xi, L->xo, L->cs})
+    if (x) cudaStreamDestroy(x);
   free_all(L);
   delete L;
 }
