@@ -224,9 +224,12 @@ moe_status moe_forward_host(moe_layer *layer, const void *hidden_host,
  * (created on the first call), both ordered after the work `stream` held at
  * the call.  Consecutive calls overlap: step i+1's input copy waits only
  * until step i's front end has read the device input buffers, and step i's
- * output copy runs while step i+1 computes.  One layer's calls must come
- * from one host thread at a time.  Errors as moe_forward; MOE_ERR_CUDA if
- * the streams cannot be created.                                          */
+ * output copy runs while step i+1 computes.  Decode-sized steps (T <= 16)
+ * whose buffers are page-locked memory the device can address skip the
+ * copies: the layer reads and writes the host buffers in place (see
+ * moe_forward_host).  One layer's calls must come from one host thread at a
+ * time.  Errors as moe_forward; MOE_ERR_CUDA if the streams cannot be
+ * created.                                                                */
 moe_status moe_forward_host_async(moe_layer *layer, const void *hidden_host,
                                   const float *router_logits_host,
                                   void *out_host, int T, void *stream);

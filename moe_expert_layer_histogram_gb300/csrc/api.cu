@@ -755,6 +755,25 @@ moe_status moe_forward_host_async(moe_layer* L, const void* hidden_host, const f
     }
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Decode-sized steps whose buffers the GPU can address in place (pinned
+  // memory over NVLink-C2C) skip the copies: the single-launch decode kernel
+  // reads the inputs and writes the output in host memory, and a step costs
+  // the host one launch instead of three copies besides.
+  if (L->host_zero_copy && T <= kSmallFrontTokens) {
+    void* hd = device_view(hidden_host);
+    void* ld = device_view(logits_host);
+    void* od = device_view(out_host);
+    if (hd && ld && od && io_aligned(hd, ld, od)) {
+      if (cudaStreamWaitEvent(L->cs, L->ev_user, 0) != cudaSuccess) return MOE_ERR_CUDA;
+      moe_status st = forward_impl(L, hd, static_cast<const float*>(ld), od, T, L->cs, nullptr,
+                                   nullptr);
+      if (st != MOE_OK) return st;
+      return cudaEventRecord(L->ev_comb, L->cs) == cudaSuccess &&
+                     cudaStreamWaitEvent(s, L->ev_comb, 0) == cudaSuccess
+                 ? MOE_OK
+                 : MOE_ERR_CUDA;
+    }
+  }
   const size_t hb = static_cast<size_t>(T) * L->H * 2, lb = static_cast<size_t>(T) * L->E * 4;
   // The input copies wait until the previous step's front end has read
   // h_in and l_in; the layer waits for them and for the latest work other
