@@ -228,7 +228,9 @@ moe_status moe_forward_host(moe_layer *layer, const void *hidden_host,
  * whose buffers are page-locked memory the device can address skip the
  * copies: the layer reads and writes the host buffers in place (see
  * moe_forward_host).  One layer's calls must come from one host thread at a
- * time.  Errors as moe_forward; MOE_ERR_CUDA if the streams cannot be
+ * time, and they cannot be captured into a CUDA graph (their work runs on
+ * the layer's own streams; capture moe_forward with device buffers
+ * instead).  Errors as moe_forward; MOE_ERR_CUDA if the streams cannot be
  * created.                                                                */
 moe_status moe_forward_host_async(moe_layer *layer, const void *hidden_host,
                                   const float *router_logits_host,

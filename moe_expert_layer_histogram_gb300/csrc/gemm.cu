@@ -27,11 +27,12 @@
 // the operands; four stager warps (12-15, one per TMEM lane quarter) write a
 // stage's scales into TMEM as soon as the stage's previous MMAs are done and
 // report on the stage's full barrier, so the MMA thread waits once per stage
-// and the staging overlaps the operand copies.  At N = 256 every K slice
-// moves about 127 KB through an SM's shared memory (54 KB of copies, 48 KB
-// of MMA operand reads, the stagers' scale reads): at 128 bytes per clock
-// that is about 490 ns, which is what a slice takes (measured 486 ns).  The
-// tensor pipe alone would take 262 ns.
+// and the staging overlaps the operand copies.  At N = 256 a K slice takes
+// the MMA thread about as long as its wait, four MMA issues, commit and
+// loop (measured ~700 cycles; the tensor pipe alone needs 524), and moves
+// about 127 KB through the SM's shared memory (54 KB of copies, 48 KB of MMA
+// operand reads, the stagers' scale reads), about 490 ns at 128 bytes per
+// clock: both limits sit near the measured ~480 ns per slice.
 // The epilogue warps (3.., or 4-11 in the 16-warp wide NVFP4 kernel) drain
 // the accumulator (tcgen05.ld), run the epilogue and store, each thread one
 // row, in whole 32-byte sectors and marked L2 evict-first.  The token tile is the
