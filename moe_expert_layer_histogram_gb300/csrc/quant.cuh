@@ -59,12 +59,24 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float* q) {
 }
 
 // ---------------------------------------------------------------- blocks
+// x / s correctly rounded, for a positive e4m3 scale value s, r = RN(1 / s)
+// and |x / s| small enough not to overflow, without a divide: q = x * r,
+// then one Newton step on the residual, q + (x - q s) r, both steps fused.
+// The residual is exact, and the step gives the correctly rounded quotient
+// for every x with |x| >= 2^-99 (checked for all fp32 significands against
+// the eight e4m3 significands; exponents only scale the steps above that).
+// Below it the quotient is under 2^-90, nowhere near an e2m1 step, and only
+// its sign matters, which is taken from x (the step alone turns -0 into +0).
+__device__ __forceinline__ float div_e4m3_scale(float x, float s, float r) {
+  const float q = __fmul_rn(x, r);
+  const float rho = __fmaf_rn(-q, s, x);
+  return copysignf(__fmaf_rn(rho, r, q), x);
+}
+
 // x[16] -> codes[2] (8 bytes, element 2j in the low nibble) and one e4m3
-// scale byte.
-// Zero dividends are answered without dividing (the quotient is the signed
-// zero itself): the correctly rounded divide is much slower on them, and a
-// squared-ReLU block is half zeros.  Blocks without zeros keep sixteen
-// independent divides (a select around each one costs their overlap).
+// scale byte.  Every element is divided by the quantised scale as above; a
+// block whose maximum is infinite (inf * r would leave a NaN residual) takes
+// correctly rounded divides instead.
 __device__ __forceinline__ void quant_nvfp4_16(const float* x, uint32_t (&codes)[2],
                                                uint8_t& sf) {
   float amax = 0.0f;
@@ -77,16 +89,14 @@ __device__ __forceinline__ void quant_nvfp4_16(const float* x, uint32_t (&codes)
     codes[0] = codes[1] = 0u;
     return;
   }
-  bool has_zero = false;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) has_zero |= x[i] == 0.0f;
   float q[16];
-  if (!has_zero) {
+  if (amax != __int_as_float(0x7F800000)) {
+    const float r = __frcp_rn(sv);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(x[i], sv);
+    for (int i = 0; i < 16; ++i) q[i] = div_e4m3_scale(x[i], sv, r);
   } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) q[i] = x[i] == 0.0f ? x[i] : __fdiv_rn(x[i], sv);
+    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(x[i], sv);
   }
   codes[0] = cvt_e2m1x8(q);
   codes[1] = cvt_e2m1x8(q + 8);

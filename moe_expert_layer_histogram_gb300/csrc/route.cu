@@ -131,22 +131,29 @@ __global__ void __launch_bounds__(1024) expert_scan_kernel(const int32_t* __rest
     }
 }
 
-// Block-wide exclusive scan of one value per thread (each thread's value
-// covering two experts; wsum holds one int per warp of the block).
-__device__ __forceinline__ int block_scan_pair(int v, int* wsum) {
+// Block-wide exclusive scans of the row counts and the 128-row chunk counts
+// of the thread's two experts, both in one pass: the pair is packed into one
+// 64-bit value (row count high, chunk count low; every partial sum of either
+// stays below 2^31, so the low half never carries).  wsum holds one value
+// per warp of the block.  The padded-row offsets are kRowBlock times the
+// chunk offsets, so they need no scan of their own.
+__device__ __forceinline__ void block_scan_counts(int rows, int chunks, uint64_t* wsum,
+                                                  int& xrows, int& xchunks) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
+  const uint64_t v = (static_cast<uint64_t>(rows) << 32) | static_cast<uint32_t>(chunks);
+  uint64_t inc = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(kFull, inc, off);
+    const uint64_t o = __shfl_up_sync(kFull, inc, off);
     if (lane >= off) inc += o;
   }
   if (lane == 31) wsum[warp] = inc;
   __syncthreads();
-  int add = 0;
+  uint64_t add = 0;
   for (int w2 = 0; w2 < warp; ++w2) add += wsum[w2];
-  __syncthreads();
-  return inc - v + add;
+  const uint64_t ex = inc - v + add;
+  xrows = static_cast<int>(ex >> 32);
+  xchunks = static_cast<int>(static_cast<uint32_t>(ex));
 }
 
 // ---------------------------------------------------------------- scatter
@@ -183,9 +190,10 @@ __global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
   pdl_launch_dependents();
   pdl_wait();
   __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts];
-  __shared__ int s_prow[kTokensPerRouteBlock * kMaxTopK], s_e[kTokensPerRouteBlock * kMaxTopK];
+  __shared__ int s_e[kTokensPerRouteBlock * kMaxTopK];
+  __shared__ RowDst s_dst[kTokensPerRouteBlock * kMaxTopK];
   constexpr int W = scatter_warps_per_token<FMT>();
-  __shared__ int wsum[scatter_threads<FMT>() / 32];
+  __shared__ uint64_t wsum[scatter_threads<FMT>() / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok0 = blockIdx.x * kTokensPerRouteBlock;
   const int ntok = min(kTokensPerRouteBlock, T - tok0);
@@ -194,9 +202,9 @@ __global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
   const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
   const int c0 = e0 < E ? counts[e0] : 0, c1 = e1 < E ? counts[e1] : 0;
   const int p0 = (c0 + kRowBlock - 1) / kRowBlock, p1 = (c1 + kRowBlock - 1) / kRowBlock;
-  const int xo = block_scan_pair(c0 + c1, wsum);
-  const int xp = block_scan_pair((p0 + p1) * kRowBlock, wsum);
-  const int xc = block_scan_pair(p0 + p1, wsum);
+  int xo, xc;
+  block_scan_counts(c0 + c1, p0 + p1, wsum, xo, xc);
+  const int xp = xc * kRowBlock;
   if (e0 < E) {
     s_off[e0] = xo;
     s_poff[e0] = xp;
@@ -241,15 +249,15 @@ __global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
     const int prow = s_poff[e] + r;
     inv[s] = prow;
     if (prow_slot) prow_slot[prow] = static_cast<int32_t>(s);
-    s_prow[j] = prow;
+    s_dst[j] = row_dst<FMT>(prow, H);
   }
   __syncthreads();
 
   // 3. GEMM1 input rows
   const int tok = warp / W, part = warp % W;
   if (tok >= ntok) return;
-  quant_row_to_rows<FMT>(hidden + static_cast<int64_t>(tok0 + tok) * H, H, s_prow + tok * K, K,
-                         xq, xsf, part * 32 + lane, 32 * W);
+  quant_row_to_rows<FMT>(hidden + static_cast<int64_t>(tok0 + tok) * H, H, RowDsts{s_dst + tok * K},
+                         K, xq, xsf, part * 32 + lane, 32 * W);
 }
 
 // ---------------------------------------------------------------- small batches
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(256) small_front_kernel(
   pdl_launch_dependents();
   __shared__ int hist[kMaxExperts], cnt[kMaxExperts], s_off[kMaxExperts], s_poff[kMaxExperts];
   __shared__ int s_ids[kSmallFrontTokens * kMaxTopK], s_prow[kSmallFrontTokens * kMaxTopK];
-  __shared__ int wsum[8];
+  __shared__ uint64_t wsum[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = cnt[e] = 0;
   __syncthreads();
@@ -298,9 +306,9 @@ __global__ void __launch_bounds__(256) small_front_kernel(
   const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
   const int c0 = e0 < E ? hist[e0] : 0, c1 = e1 < E ? hist[e1] : 0;
   const int p0 = (c0 + kRowBlock - 1) / kRowBlock, p1 = (c1 + kRowBlock - 1) / kRowBlock;
-  const int xo = block_scan_pair(c0 + c1, wsum);
-  const int xp = block_scan_pair((p0 + p1) * kRowBlock, wsum);
-  const int xc = block_scan_pair(p0 + p1, wsum);
+  int xo, xc;
+  block_scan_counts(c0 + c1, p0 + p1, wsum, xo, xc);
+  const int xp = xc * kRowBlock;
   if (e0 < E) {
     s_off[e0] = xo;
     s_poff[e0] = xp;
@@ -377,7 +385,7 @@ __global__ void __launch_bounds__(256) batched_quant_kernel(
     uint8_t* __restrict__ xsf, int* status) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ int wsum[8];
+  __shared__ uint64_t wsum[8];
   __shared__ int s_base, s_cnt;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.y;
@@ -388,9 +396,9 @@ __global__ void __launch_bounds__(256) batched_quant_kernel(
   c0 = min(max(c0, 0), M);
   c1 = min(max(c1, 0), M);
   const int p0 = (c0 + kRowBlock - 1) / kRowBlock, p1 = (c1 + kRowBlock - 1) / kRowBlock;
-  const int xo = block_scan_pair(c0 + c1, wsum);
-  const int xp = block_scan_pair((p0 + p1) * kRowBlock, wsum);
-  const int xc = block_scan_pair(p0 + p1, wsum);
+  int xo, xc;
+  block_scan_counts(c0 + c1, p0 + p1, wsum, xo, xc);
+  const int xp = xc * kRowBlock;
   if (e0 == e) {
     s_base = xp;
     s_cnt = c0;
@@ -422,8 +430,8 @@ __global__ void __launch_bounds__(256) batched_quant_kernel(
   const int r = blockIdx.x * kTokensPerRouteBlock + warp;
   if (r >= s_cnt) return;
   const int prow = s_base + r;
-  quant_row_to_rows<FMT>(hidden + (static_cast<int64_t>(e) * M + r) * H, H, &prow, 1, xq, xsf,
-                         lane);
+  quant_row_to_rows<FMT>(hidden + (static_cast<int64_t>(e) * M + r) * H, H, PaddedRows{&prow, H}, 1,
+                         xq, xsf, lane);
 }
 
 // ---------------------------------------------------------------- combine

@@ -54,40 +54,79 @@ __device__ __forceinline__ void unpack_bf16(const uint4* src, float (&f)[N]) {
   }
 }
 
-// Unit `u` of a token row, already loaded, into the padded rows prows[0..n):
-// BF16 copied, MXFP8 / NVFP4 quantised, codes row-major and scales in the
-// MMA's 128-row scale tiles.
+// Where one padded row's GEMM1 input goes: the byte offset of its codes and
+// the unit-independent part of its scale bytes' offset in the scale tiles
+// (sf_tile_offset(prow, u, tiles_k) is that part plus (u / 4) * 512 + u % 4).
+struct RowDst {
+  int64_t code;
+  int64_t sf;
+};
+
 template <int FMT>
-__device__ __forceinline__ void store_unit_rows(const RawUnit<FMT>& r, int H, int u,
-                                                const int* prows, int n,
-                                                uint8_t* __restrict__ xq,
+__device__ __forceinline__ RowDst row_dst(int prow, int H) {
+  const int64_t p = prow;
+  if constexpr (FMT == kFmtBF16) return RowDst{p * H * 2, 0};
+  else if constexpr (FMT == kFmtNVFP4) return RowDst{p * (H / 2), sf_tile_offset(p, 0, H / 64)};
+  else return RowDst{p * H, sf_tile_offset(p, 0, H / 128)};
+}
+
+// Destinations given as padded row numbers.
+struct PaddedRows {
+  const int* prows;
+  int H;
+  template <int FMT>
+  __device__ __forceinline__ RowDst get(int k) const {
+    return row_dst<FMT>(prows[k], H);
+  }
+};
+
+// Destinations precomputed once per row (row_dst).
+struct RowDsts {
+  const RowDst* d;
+  template <int FMT>
+  __device__ __forceinline__ RowDst get(int k) const {
+    return d[k];
+  }
+};
+
+// Unit `u` of a token row, already loaded, into the n padded rows `dst`
+// names: BF16 copied, MXFP8 / NVFP4 quantised, codes row-major and scales in
+// the MMA's 128-row scale tiles.
+template <int FMT, class Dst>
+__device__ __forceinline__ void store_unit_rows(const RawUnit<FMT>& r, int u, const Dst& dst,
+                                                int n, uint8_t* __restrict__ xq,
                                                 uint8_t* __restrict__ xsf) {
   if constexpr (FMT == kFmtBF16) {
     for (int k = 0; k < n; ++k)
-      reinterpret_cast<uint4*>(xq + static_cast<int64_t>(prows[k]) * H * 2)[u] = r.v[0];
-  } else if constexpr (FMT == kFmtNVFP4) {
-    float f[16];
-    unpack_bf16<16>(r.v, f);
-    uint32_t codes[2];
-    uint8_t sf;
-    quant_nvfp4_16(f, codes, sf);
-    for (int k = 0; k < n; ++k) {
-      const int64_t prow = prows[k];
-      *reinterpret_cast<uint2*>(xq + prow * (H / 2) + u * 8) = make_uint2(codes[0], codes[1]);
-      xsf[sf_tile_offset(prow, u, H / 64)] = sf;
-    }
+      reinterpret_cast<uint4*>(xq + dst.template get<FMT>(k).code)[u] = r.v[0];
   } else {
-    float f[32];
-    unpack_bf16<32>(r.v, f);
-    uint32_t codes[8];
-    uint8_t sf;
-    quant_mxfp8_32(f, codes, sf);
-    for (int k = 0; k < n; ++k) {
-      const int64_t prow = prows[k];
-      uint4* dst = reinterpret_cast<uint4*>(xq + prow * H + u * 32);
-      dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-      dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-      xsf[sf_tile_offset(prow, u, H / 128)] = sf;
+    constexpr int kUnitBytes = FMT == kFmtNVFP4 ? 8 : 32;
+    const int64_t cu = static_cast<int64_t>(u) * kUnitBytes;
+    const int su = (u >> 2) * 512 + (u & 3);
+    if constexpr (FMT == kFmtNVFP4) {
+      float f[16];
+      unpack_bf16<16>(r.v, f);
+      uint32_t codes[2];
+      uint8_t sf;
+      quant_nvfp4_16(f, codes, sf);
+      for (int k = 0; k < n; ++k) {
+        const RowDst d = dst.template get<FMT>(k);
+        *reinterpret_cast<uint2*>(xq + d.code + cu) = make_uint2(codes[0], codes[1]);
+        xsf[d.sf + su] = sf;
+      }
+    } else {
+      float f[32];
+      unpack_bf16<32>(r.v, f);
+      uint32_t codes[8];
+      uint8_t sf;
+      quant_mxfp8_32(f, codes, sf);
+      for (int k = 0; k < n; ++k) {
+        const RowDst d = dst.template get<FMT>(k);
+        uint4* out = reinterpret_cast<uint4*>(xq + d.code + cu);
+        out[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        out[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        xsf[d.sf + su] = sf;
+      }
     }
   }
 }
@@ -99,7 +138,7 @@ __device__ __forceinline__ void quant_unit_to_rows(const __nv_bfloat16* __restri
                                                    uint8_t* __restrict__ xsf) {
   RawUnit<FMT> r;
   load_unit<FMT>(x, u, r);
-  store_unit_rows<FMT>(r, H, u, prows, n, xq, xsf);
+  store_unit_rows<FMT>(r, u, PaddedRows{prows, H}, n, xq, xsf);
 }
 
 // Writes the GEMM1 input of one token row into its padded rows: this thread
@@ -107,9 +146,9 @@ __device__ __forceinline__ void quant_unit_to_rows(const __nv_bfloat16* __restri
 // 32).  The next unit's load is issued before the current one is quantised
 // and stored, so each thread keeps two loads in flight instead of waiting out
 // the latency of every one.
-template <int FMT>
+template <int FMT, class Dst>
 __device__ __forceinline__ void quant_row_to_rows(const __nv_bfloat16* __restrict__ x, int H,
-                                                  const int* prows, int n,
+                                                  const Dst& dst, int n,
                                                   uint8_t* __restrict__ xq,
                                                   uint8_t* __restrict__ xsf, int first,
                                                   int stride = 32) {
@@ -121,7 +160,7 @@ __device__ __forceinline__ void quant_row_to_rows(const __nv_bfloat16* __restric
     RawUnit<FMT> nxt;
     const bool more = u + stride < U;
     if (more) load_unit<FMT>(x, u + stride, nxt);
-    store_unit_rows<FMT>(cur, H, u, prows, n, xq, xsf);
+    store_unit_rows<FMT>(cur, u, dst, n, xq, xsf);
     if (more) cur = nxt;
   }
 }
