@@ -45,6 +45,8 @@ struct moe_layer {
   float* acc = nullptr;              // in-kernel reduce: fp32 [Tmax, H], zero between forwards
   int32_t *acc_cnt = nullptr, *prow_slot = nullptr;
   int32_t* done1 = nullptr;          // fused decode GEMMs: per-expert GEMM1 completion counts
+  int32_t* otab = nullptr;           // [4(E+1)] the GEMMs' item tables in the mixed order
+  int mix_items = 1;                 // wide single-CTA GEMMs: single-chunk experts' items mixed in
   DecodeCtl* dctl = nullptr;         // single-launch decode: counters (zero between forwards)
   int single_launch = 1;             // T <= 16: the whole layer in one kernel
   int fused_gemms = 1;               // T <= 16: GEMM1 and GEMM2 in one launch
@@ -190,11 +192,25 @@ void set_pdl(const moe_layer* L, bool wide) {
 
 // GEMM1 (+ the activation and re-quantisation) over the padded
 // activation rows of the current tables.
-GemmArgs gemm1_args(const moe_layer* L, int pair, bool wide) {
+// The item tables of a GEMM launch: by expert, or (mixed) the ones the
+// scatter kernel wrote in the mixed order.
+void set_tables(const moe_layer* L, bool mixed, GemmArgs& a) {
+  if (mixed) {
+    a.chunk_off = L->otab;
+    a.pad_off = L->otab + (L->E + 1);
+    a.counts = L->otab + (2 * L->E + 1);
+    a.order = L->otab + (3 * L->E + 1);
+  } else {
+    a.chunk_off = L->chunk_off;
+    a.pad_off = L->pad_off;
+    a.counts = L->counts;
+    a.order = nullptr;
+  }
+}
+
+GemmArgs gemm1_args(const moe_layer* L, int pair, bool wide, bool mixed = false) {
   GemmArgs a{};
-  a.chunk_off = L->chunk_off;
-  a.pad_off = L->pad_off;
-  a.counts = L->counts;
+  set_tables(L, mixed, a);
   a.E = L->E;
   a.n_tiles = L->w13_rows / (wide ? 256 : 128);
   a.num_kb = L->xb / 128;
@@ -220,11 +236,9 @@ GemmArgs gemm1_args(const moe_layer* L, int pair, bool wide) {
 // with the in-kernel reduce): the bf16 layer output, summed by GEMM2's
 // epilogue instead of the combine kernel.
 GemmArgs gemm2_args(const moe_layer* L, int pair, bool wide, void* out, int rows_per_expert,
-                    void* reduce_out) {
+                    void* reduce_out, bool mixed = false) {
   GemmArgs a{};
-  a.chunk_off = L->chunk_off;
-  a.pad_off = L->pad_off;
-  a.counts = L->counts;
+  set_tables(L, mixed, a);
   a.E = L->E;
   a.n_tiles = L->H / (wide ? 256 : 128);
   a.num_kb = L->hb / 128;
@@ -269,18 +283,21 @@ cudaError_t launch_wide_or_pair(moe_layer* L, int epi, const GemmMaps& maps, con
 }
 
 // max_rows bounds the rows of any expert (selects the activation tile height).
+// mixed: the scatter kernel wrote the mixed-order tables (wide single-CTA
+// launches of the routed forward).
 cudaError_t run_gemm1(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide,
-                      cudaStream_t s) {
+                      cudaStream_t s, bool mixed = false) {
   wide = wide && L->w13_rows % 256 == 0;
-  const GemmArgs a = gemm1_args(L, pair, wide);
+  const GemmArgs a = gemm1_args(L, pair, wide, mixed && wide);
   return launch_wide_or_pair(L, L->act == MOE_ACT_RELU2 ? 3 : 1, L->maps1, a, chunks, max_rows,
                              wide, s);
 }
 
 cudaError_t run_gemm2(moe_layer* L, int64_t chunks, int max_rows, int pair, bool wide, void* out,
-                      int rows_per_expert, cudaStream_t s, void* reduce_out = nullptr) {
+                      int rows_per_expert, cudaStream_t s, void* reduce_out = nullptr,
+                      bool mixed = false) {
   wide = wide && L->H % 256 == 0;
-  const GemmArgs a = gemm2_args(L, pair, wide, out, rows_per_expert, reduce_out);
+  const GemmArgs a = gemm2_args(L, pair, wide, out, rows_per_expert, reduce_out, mixed && wide);
   return launch_wide_or_pair(L, 2, L->maps2, a, chunks, max_rows, wide, s);
 }
 
@@ -430,6 +447,9 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
   if (const char* fv = std::getenv("MOE_FUSED_GEMMS")) L->fused_gemms = fv[0] != '0';
   // MOE_HOST_ZERO_COPY=0: moe_forward_host always copies through device buffers.
   if (const char* zv = std::getenv("MOE_HOST_ZERO_COPY")) L->host_zero_copy = zv[0] != '0';
+  // MOE_MIX_ITEMS=0: wide GEMM launches take their items in plain expert
+  // order instead of mixing the single-chunk experts' items in.
+  if (const char* mv = std::getenv("MOE_MIX_ITEMS")) L->mix_items = mv[0] != '0';
   const int H = L->H, I = L->I, E = L->E;
   if (L->fmt == MOE_FMT_NVFP4) {
     L->xb = H / 2; L->hb = I / 2; L->x_tiles_k = H / 64; L->h_tiles_k = I / 64;
@@ -460,7 +480,8 @@ moe_status moe_create(const moe_config* cfg, moe_layer** out) {
             A.get(&L->l_in, static_cast<size_t>(L->Tmax) * E * 4) &&
             A.get(&L->o_out, static_cast<size_t>(L->Tmax) * H * 2) &&
             A.get(&L->done1, static_cast<size_t>(E) * 4) &&
-            A.get(&L->dctl, sizeof(DecodeCtl));
+            A.get(&L->dctl, sizeof(DecodeCtl)) &&
+            A.get(&L->otab, static_cast<size_t>(E + 1) * 4 * 4);
   const bool reduce = L->combine == MOE_COMBINE_REDUCE;
   const bool counted = L->combine != MOE_COMBINE_GATHER;  // reduce or fused combine
   ok = ok && (!reduce || A.get(&L->acc, static_cast<size_t>(L->Tmax) * H * 4));
@@ -556,6 +577,9 @@ moe_status forward_impl(moe_layer* L, const void* hidden, const float* logits, v
   int launches = 4;
   const bool small = T <= kSmallFrontTokens;
   const bool wide = L->wide_tiles == 1 || (L->wide_tiles < 0 && T > kPairCopyMaxTokens);
+  // single-chunk experts' items mixed into the wide single-CTA GEMMs (the
+  // CTA-pair kernels map items by expert)
+  const bool mixed = L->mix_items && wide && !small && L->pair_clusters == 0;
   set_pdl(L, wide);
   // (the fused combine has the decode kernel's own combine for T <= 16)
   if (small && L->single_launch && L->fused_gemms && L->combine != MOE_COMBINE_REDUCE &&
@@ -614,7 +638,7 @@ moe_status forward_impl(moe_layer* L, const void* hidden, const float* logits, v
     if (e == cudaSuccess)
       e = launch_scatter_quant(L->fmt, L->ids, T, E, K, hidden, H, L->prefix, L->counts,
                                L->offsets, L->pad_off, L->chunk_off, L->perm, L->inv,
-                               L->prow_slot, L->xq, L->xsf, s);
+                               L->prow_slot, mixed ? L->otab : nullptr, L->xq, L->xsf, s);
     launches = 6;
   }
   if (front_done) cudaEventRecord(front_done, s);
@@ -633,9 +657,9 @@ moe_status forward_impl(moe_layer* L, const void* hidden, const float* logits, v
     --launches;
     mark(4);
   } else {
-    if (e == cudaSuccess) e = run_gemm1(L, chunks, T, pair, wide, s);
+    if (e == cudaSuccess) e = run_gemm1(L, chunks, T, pair, wide, s, mixed);
     mark(4);
-    if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, wide, L->y, 0, s, out);
+    if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, wide, L->y, 0, s, out, mixed);
   }
   mark(5);
   // with the in-kernel reduce or the fused combine GEMM2 has written `out` already

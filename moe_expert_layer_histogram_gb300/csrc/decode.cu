@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const Tables tab{S.tab, S.tab + (E + 1), S.tab + (2 * E + 1)};
+  const Tables tab{S.tab, S.tab + (E + 1), S.tab + (2 * E + 1), nullptr};
   const int n1 = S.tab[E] * a1.n_tiles;
   const int total = n1 + S.tab[E] * a2.n_tiles;
   auto second = [&](int item) { return item >= n1; };
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           // are the quantised tokens
           const int* counter = second(item) ? ctl->done1 + it.e : &ctl->qdone;
           const int need =
-              second(item) ? 4 * a1.n_tiles * (tab.chunk_off[it.e + 1] - tab.chunk_off[it.e])
+              second(item) ? 4 * a1.n_tiles * (tab.chunk_off[it.k + 1] - tab.chunk_off[it.k])
                          : T * segs;
           if (ld_acquire(counter) < need) {
             // start the weight stream before waiting for the activations

@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sf_ready + kStages + (WS ? 2 * kStages : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_tab = reinterpret_cast<int*>(tmem_holder + 4);
-  const Tables tab{s_tab, s_tab + (args.E + 1), s_tab + (2 * args.E + 1)};
+  const Tables tab{s_tab, s_tab + (args.E + 1), s_tab + (2 * args.E + 1),
+                   args.order ? s_tab + (3 * args.E + 1) : nullptr};
   pdl_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -153,6 +154,8 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
     s_tab[args.E + 1 + i] = args.pad_off[i];
     s_tab[2 * args.E + 1 + i] = args.counts[i];
   }
+  if (args.order)
+    for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_tab[3 * args.E + 1 + i] = args.order[i];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
           }
           if (second(item)) {
             // GEMM2's activations are GEMM1's output for this expert
-            const int need = 4 * args.n_tiles * (tab.chunk_off[it.e + 1] - tab.chunk_off[it.e]);
+            const int need = 4 * args.n_tiles * (tab.chunk_off[it.k + 1] - tab.chunk_off[it.k]);
             if (!wait_count_at_least(args.done1 + it.e, need, abort_flag)) {
               ok = false;
               break;
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
             fence_proxy_async_global();  // generic-proxy stores -> the TMA reads below
           }
           const uint64_t policy =
-              tab.chunk_off[it.e + 1] - tab.chunk_off[it.e] > 1 ? reused : once;
+              tab.chunk_off[it.k + 1] - tab.chunk_off[it.k] > 1 ? reused : once;
           // WS: operand codes only (the scale ring carries the scale tiles)
           const uint32_t bytes = WS ? (16u << amap) * 128u + NW * kTileBytes
                                     : (16u << amap) * 128u + NW * A.b_tile_bytes + SFT * 512u;
@@ -359,7 +362,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
           const GemmArgs& A = gargs(item);
           const Item it = map_item(tab, args.E, A.n_tiles, local_item(item));
           const uint64_t policy =
-              tab.chunk_off[it.e + 1] - tab.chunk_off[it.e] > 1 ? reused : once;
+              tab.chunk_off[it.k + 1] - tab.chunk_off[it.k] > 1 ? reused : once;
           const uint8_t* sfa = A.sfa + static_cast<int64_t>(it.prow0 >> 7) * A.sfa_tiles_k * 512;
           const uint8_t* btile =
               A.b_tiles + (static_cast<int64_t>(it.e) * A.n_tiles + it.n_tile) * NW * A.num_kb *
@@ -652,7 +655,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
       // batched format: expert e's rows go to rows e*M.. of the output
       const int64_t orow = A.out_rows_per_expert
                                ? static_cast<int64_t>(it.e) * A.out_rows_per_expert +
-                                     (it.prow0 - tab.pad_off[it.e]) + r
+                                     (it.prow0 - tab.pad_off[it.k]) + r
                                : prow;
       const int n128 = it.n_tile * NW + grp;
       if constexpr (NW == 1) {

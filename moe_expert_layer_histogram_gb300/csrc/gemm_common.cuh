@@ -53,8 +53,8 @@ struct Fmt<kFmtNVFP4> {
 };
 
 // Per-expert item tables kept in shared memory: chunk_off[E+1],
-// pad_off[E], counts[E].
-constexpr int kTableInts = 3 * (kMaxExperts + 1);
+// pad_off[E], counts[E] and the expert order order[E+1].
+constexpr int kTableInts = 4 * (kMaxExperts + 1);
 constexpr int kSmemLimit = 232448;  // opt-in maximum per block
 
 // A stage holds the activation tile (MROWS rows x 128 bytes), the NW weight
@@ -95,30 +95,70 @@ constexpr int kSplitLaunchRegs = (2 * kLeanRegs + 2 * kEpiRegs) / 4;
 static_assert(kSplitLaunchRegs * 512 <= 65536, "register split exceeds the register file");
 
 struct Item {
-  int e, n_tile, prow0, rows;
+  int e;       // expert (its weight tiles)
+  int k;       // its position in the tables
+  int n_tile, prow0, rows;
 };
 
-// Work item -> (expert, weight tile, chunk).  Items are numbered expert-major:
-// expert e owns items [chunk_off[e] * n_tiles, chunk_off[e+1] * n_tiles).
-// The tables live in shared memory (loaded once per CTA).
+// Work item -> (expert, weight tile, chunk).  Items are numbered in table
+// order: the expert at table position k owns items [chunk_off[k] * n_tiles,
+// chunk_off[k+1] * n_tiles), weight tile major, chunk minor, so that the
+// CTAs working at the same time share a weight tile through L2.  Without
+// an order table, position k is expert k.  With one (wide launches), the
+// experts with several chunks come first (in expert order), then those with
+// one chunk at most, and the single-chunk experts' items are spread evenly
+// among the others (below).  The tables live in shared memory (loaded once
+// per CTA).
 struct Tables {
   const int* chunk_off;  // [E+1]
   const int* pad_off;    // [E]
   const int* counts;     // [E]
+  const int* order;      // [E+1]: expert at each position, then the chunks of
+                         // the multi-chunk positions; nullptr: the identity
 };
 
+// A single-chunk expert's weight tiles are read from DRAM once, by one item
+// each, while a multi-chunk expert's tiles are read once and then served
+// from L2 to its other chunks.  In plain table order the CTAs meet long runs
+// of single-chunk items (DRAM-bound, the tensor pipes idle) and long runs of
+// multi-chunk items (the reverse).  Mixed in at an even rate (item i is the
+// c-th single-chunk item when floor((i+1) nc / n) > c = floor(i nc / n)),
+// the weight streams overlap the tensor work.  A bijection on [0, n).
+// floor(a b / n) for 0 <= a, b <= n, without an integer divide: a float
+// estimate (within one of the result for n below 2^20), then corrected.
+__device__ __forceinline__ int floor_mul_div(int a, int b, int n) {
+  int q = static_cast<int>(__fdividef(static_cast<float>(a) * static_cast<float>(b),
+                                      static_cast<float>(n)));
+  const int64_t p = static_cast<int64_t>(a) * b;
+  while (q > 0 && static_cast<int64_t>(q) * n > p) --q;
+  while (static_cast<int64_t>(q + 1) * n <= p) ++q;
+  return q;
+}
+
+__device__ __forceinline__ int mix_item(const Tables& t, int E, int n_tiles, int item) {
+  if (t.order == nullptr) return item;
+  const int n = t.chunk_off[E] * n_tiles;
+  const int nh = t.order[E] * n_tiles;
+  const int nc = n - nh;
+  if (nc <= 0 || nh <= 0) return item;
+  const int c0 = floor_mul_div(item, nc, n), c1 = floor_mul_div(item + 1, nc, n);
+  return c1 > c0 ? nh + c0 : item - c0;
+}
+
 __device__ __forceinline__ Item map_item(const Tables& t, int E, int n_tiles, int item) {
-  int lo = 0, hi = E;  // chunk_off[lo]*nt <= item < chunk_off[hi]*nt
+  const int g = mix_item(t, E, n_tiles, item);
+  int lo = 0, hi = E;  // chunk_off[lo]*nt <= g < chunk_off[hi]*nt
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (t.chunk_off[mid] * n_tiles <= item) lo = mid; else hi = mid;
+    if (t.chunk_off[mid] * n_tiles <= g) lo = mid; else hi = mid;
   }
   const int c0 = t.chunk_off[lo];
   const int nch = t.chunk_off[lo + 1] - c0;
-  const int local = item - c0 * n_tiles;
+  const int local = g - c0 * n_tiles;
   const int chunk = local % nch;
   Item it;
-  it.e = lo;
+  it.e = t.order ? t.order[lo] : lo;
+  it.k = lo;
   it.n_tile = local / nch;
   it.prow0 = t.pad_off[lo] + chunk * kRowBlock;
   it.rows = min(kRowBlock, t.counts[lo] - chunk * kRowBlock);

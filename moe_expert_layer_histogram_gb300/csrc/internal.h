@@ -34,6 +34,10 @@ struct GemmArgs {
   const int32_t* chunk_off;  // [E+1] exclusive scan of ceil(count/128)
   const int32_t* pad_off;    // [E+1] exclusive scan of round_up(count,128)
   const int32_t* counts;     // [E]
+  // [E+1] or null: the three tables above are by table position and this is
+  // the expert at each position, then the multi-chunk positions' chunks
+  // (the mixed item order, gemm_common.cuh); null: position = expert
+  const int32_t* order;
   int E;
   int n_tiles;               // output tiles per expert
   int num_kb;                // 128-byte K stages per item
@@ -183,11 +187,14 @@ cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids,
 cudaError_t launch_expert_scan(const int32_t* blockhist, int NB, int E, int32_t* prefix,
                                int32_t* counts, cudaStream_t s);
 // prow_slot (may be null): padded row -> slot, for the in-kernel reduce.
+// otab (may be null): [4E+2] the GEMMs' item tables in the mixed order
+// (GemmArgs::order).
 cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int K,
                                  const void* hidden, int H, const int32_t* prefix,
                                  const int32_t* counts, int32_t* offsets, int32_t* pad_off,
                                  int32_t* chunk_off, int32_t* perm, int32_t* inv,
-                                 int32_t* prow_slot, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+                                 int32_t* prow_slot, int32_t* otab, uint8_t* xq, uint8_t* xsf,
+                                 cudaStream_t s);
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int K, int H,
                            void* out, cudaStream_t s);
 // T <= kSmallFrontTokens: routing, scans, ranks and GEMM1 input in one block.

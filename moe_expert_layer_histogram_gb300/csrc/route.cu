@@ -26,6 +26,9 @@ namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
+// Experts with at least this many 128-row chunks form the GEMMs' main item
+// stream; the single-chunk ones are mixed into it (store_mixed_tables).
+constexpr int kMixMinChunks = 2;
 
 // ---------------------------------------------------------------- routing
 // One warp per token (route_token), 8 tokens per block.  Block b also counts
@@ -156,6 +159,54 @@ __device__ __forceinline__ void block_scan_counts(int rows, int chunks, uint64_t
   xchunks = static_cast<int>(static_cast<uint32_t>(ex));
 }
 
+// The GEMMs' item tables in the mixed order (gemm_common.cuh, mix_item):
+// the experts with at least two chunks first, then the others, each group in
+// expert order.  otab = chunk_off[E+1], pad_off[E], counts[E] by table
+// position, then order[E+1]: the expert at each position and the number of
+// chunks of the multi-chunk group.  One block writes them; every thread
+// holds experts 2t, 2t+1 (c = rows, p = chunks, xp = first padded row of
+// expert 2t).
+__device__ __forceinline__ void store_mixed_tables(int E, int c0, int c1, int p0, int p1, int xp,
+                                                   uint64_t* wsum, int32_t* __restrict__ otab) {
+  __shared__ int s_tot[2];
+  const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
+  const int h0 = p0 >= kMixMinChunks, h1 = p1 >= kMixMinChunks;
+  int xhe, xhc, xle, xlc;  // exclusive: multi-chunk experts / their chunks, the rest
+  __syncthreads();         // wsum is reused
+  block_scan_counts(h0 + h1, h0 * p0 + h1 * p1, wsum, xhe, xhc);
+  __syncthreads();
+  block_scan_counts(2 - h0 - h1, (1 - h0) * p0 + (1 - h1) * p1, wsum, xle, xlc);
+  if (e0 == E - 1 || e1 == E - 1) {
+    // the last thread with experts: totals of the multi-chunk group (an
+    // expert 2t+1 >= E has no chunks and does not count)
+    const int h1v = e1 < E ? h1 : 0;
+    s_tot[0] = xhe + h0 + h1v;
+    s_tot[1] = xhc + h0 * p0 + h1v * p1;
+  }
+  __syncthreads();
+  const int nhe = s_tot[0], nhc = s_tot[1];
+  int32_t* o_chunk = otab;
+  int32_t* o_pad = otab + (E + 1);
+  int32_t* o_cnt = otab + (2 * E + 1);
+  int32_t* o_ord = otab + (3 * E + 1);
+  if (e0 < E) {
+    const int k = h0 ? xhe : nhe + xle;
+    o_chunk[k] = h0 ? xhc : nhc + xlc;
+    o_pad[k] = xp;
+    o_cnt[k] = c0;
+    o_ord[k] = e0;
+  }
+  if (e1 < E) {
+    const int k = h1 ? xhe + h0 : nhe + xle + (1 - h0);
+    o_chunk[k] = h1 ? xhc + h0 * p0 : nhc + xlc + (1 - h0) * p0;
+    o_pad[k] = xp + p0 * kRowBlock;
+    o_cnt[k] = c1;
+    o_ord[k] = e1;
+  }
+  if (threadIdx.x == 0) o_ord[E] = nhc;
+  if (e0 == E - 1 || e1 == E - 1) o_chunk[E] = nhc + xlc + (1 - h0) * p0 + (1 - h1) * p1;
+}
+
 // ---------------------------------------------------------------- scatter
 // Block b handles the 8 tokens of routing block b.
 //  1. Exclusive scans of the per-expert counts, 128-padded counts and 128-row
@@ -186,7 +237,7 @@ __global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
     int H, const int32_t* __restrict__ prefix, const int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ pad_off, int32_t* __restrict__ chunk_off,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ prow_slot,
-    uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
+    int32_t* __restrict__ otab, uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts];
@@ -229,6 +280,7 @@ __global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
       pad_off[E] = xp + (p0 + p1) * kRowBlock;
       chunk_off[E] = xc + p0 + p1;
     }
+    if (otab) store_mixed_tables(E, c0, c1, p0, p1, xp, wsum, otab);
   }
   __syncthreads();
 
@@ -554,7 +606,8 @@ cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int 
                                  const void* hidden, int H, const int32_t* prefix,
                                  const int32_t* counts, int32_t* offsets, int32_t* pad_off,
                                  int32_t* chunk_off, int32_t* perm, int32_t* inv,
-                                 int32_t* prow_slot, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+                                 int32_t* prow_slot, int32_t* otab, uint8_t* xq, uint8_t* xsf,
+                                 cudaStream_t s) {
   const int nb = (T + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
   const auto* hb = static_cast<const __nv_bfloat16*>(hidden);
   auto k = fmt == kFmtBF16 ? scatter_quant_kernel<kFmtBF16>
@@ -564,7 +617,7 @@ cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int 
                       : fmt == kFmtMXFP8 ? scatter_threads<kFmtMXFP8>()
                                          : scatter_threads<kFmtNVFP4>();
   return launch_pdl(g_pdl_small, k, dim3(nb), dim3(threads), 0, s, ids, T, E, K, hb, H, prefix,
-                    counts, offsets, pad_off, chunk_off, perm, inv, prow_slot, xq, xsf);
+                    counts, offsets, pad_off, chunk_off, perm, inv, prow_slot, otab, xq, xsf);
 }
 
 cudaError_t launch_small_front(int fmt, const float* logits, int T, int E, int K,
