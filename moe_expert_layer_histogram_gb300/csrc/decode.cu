@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (item < 0) break;
         const GemmArgs& A = gargs(item);
         const CUtensorMap* amaps = second(item) ? maps2.a : maps1.a;
-        const Item it = map_item(tab, E, A.n_tiles, local_item(item));
+        const Item it = map_item<false>(tab, E, A.n_tiles, local_item(item));
         const int amap = it.rows <= 16 ? 0 : 1;
         const uint32_t bytes = (16u << amap) * 128u + A.b_tile_bytes + SFT * 512u;
         const uint8_t* sfa = A.sfa + static_cast<int64_t>(it.prow0 >> 7) * A.sfa_tiles_k * 512;
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (item < 0) break;
       const GemmArgs& A = gargs(item);
       const bool g2 = second(item);
-      const Item it = map_item(tab, E, A.n_tiles, local_item(item));
+      const Item it = map_item<false>(tab, E, A.n_tiles, local_item(item));
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(&tfull[buf], use & 1u, abort_flag)) {

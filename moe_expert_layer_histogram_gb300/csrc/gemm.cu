@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_tab = reinterpret_cast<int*>(tmem_holder + 4);
   const Tables tab{s_tab, s_tab + (args.E + 1), s_tab + (2 * args.E + 1),
-                   args.order ? s_tab + (3 * args.E + 1) : nullptr};
+                   NW == 2 && args.order ? s_tab + (3 * args.E + 1) : nullptr};
   pdl_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
     s_tab[args.E + 1 + i] = args.pad_off[i];
     s_tab[2 * args.E + 1 + i] = args.counts[i];
   }
-  if (args.order)
+  if (NW == 2 && args.order)
     for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_tab[3 * args.E + 1 + i] = args.order[i];
   tc_fence_before();
   __syncthreads();
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
         bool ok = true;
         for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
           const GemmArgs& A = gargs(item);
-          const bool q0 = map_item(tab, args.E, A.n_tiles, local_item(item)).rows <= 32;
+          const bool q0 = map_item<NW == 2>(tab, args.E, A.n_tiles, local_item(item)).rows <= 32;
           for (int kb = 0; kb < A.num_kb; ++kb) {
             const bool landed = mbar_wait(&full[stage], phase, abort_flag);
             if (!__all_sync(0xFFFFFFFFu, landed)) {
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
         for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
           const GemmArgs& A = gargs(item);
           const CUtensorMap* amaps = second(item) ? maps2.a : maps.a;
-          const Item it = map_item(tab, args.E, A.n_tiles, local_item(item));
+          const Item it = map_item<NW == 2>(tab, args.E, A.n_tiles, local_item(item));
           const int amap = it.rows <= 16 ? 0 : it.rows <= 32 ? 1 : it.rows <= 64 ? 2 : 3;
           if ((16 << amap) > MROWS) {   // the host bounded the rows per chunk by MROWS
             ok = false;
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
         bool ok = true;
         for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
           const GemmArgs& A = gargs(item);
-          const Item it = map_item(tab, args.E, A.n_tiles, local_item(item));
+          const Item it = map_item<NW == 2>(tab, args.E, A.n_tiles, local_item(item));
           const uint64_t policy =
               tab.chunk_off[it.k + 1] - tab.chunk_off[it.k] > 1 ? reused : once;
           const uint8_t* sfa = A.sfa + static_cast<int64_t>(it.prow0 >> 7) * A.sfa_tiles_k * 512;
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
           // shared memory and only feed accumulator rows that are not stored).
           // Larger chunks broadcast every tile to all four quarters.
           const bool q0_only = NW == 1 && args.pair_scale_copies &&
-                               map_item(tab, args.E, A.n_tiles, local_item(item)).rows <= 32;
+                               map_item<NW == 2>(tab, args.E, A.n_tiles, local_item(item)).rows <= 32;
           if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -639,7 +639,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++local) {
       const GemmArgs& A = gargs(item);
       const bool g2 = second(item);
-      const Item it = map_item(tab, args.E, A.n_tiles, local_item(item));
+      const Item it = map_item<NW == 2>(tab, args.E, A.n_tiles, local_item(item));
       const int buf = local % kBufs;
       const uint32_t use = static_cast<uint32_t>(local / kBufs);
       if (!mbar_wait(&tfull[buf], use & 1u, abort_flag)) {

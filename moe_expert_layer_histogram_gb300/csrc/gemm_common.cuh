@@ -145,8 +145,12 @@ __device__ __forceinline__ int mix_item(const Tables& t, int E, int n_tiles, int
   return c1 > c0 ? nh + c0 : item - c0;
 }
 
+// kOrdered: the kernel may be given an order table (the wide kernels); the
+// narrow ones map by expert and carry none of it (a few registers more in
+// every narrow GEMM measured 3 % on the stream-launched bf16 T = 512 layer).
+template <bool kOrdered>
 __device__ __forceinline__ Item map_item(const Tables& t, int E, int n_tiles, int item) {
-  const int g = mix_item(t, E, n_tiles, item);
+  const int g = kOrdered ? mix_item(t, E, n_tiles, item) : item;
   int lo = 0, hi = E;  // chunk_off[lo]*nt <= g < chunk_off[hi]*nt
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -157,7 +161,7 @@ __device__ __forceinline__ Item map_item(const Tables& t, int E, int n_tiles, in
   const int local = g - c0 * n_tiles;
   const int chunk = local % nch;
   Item it;
-  it.e = t.order ? t.order[lo] : lo;
+  it.e = kOrdered && t.order ? t.order[lo] : lo;
   it.k = lo;
   it.n_tile = local / nch;
   it.prow0 = t.pad_off[lo] + chunk * kRowBlock;
