@@ -280,7 +280,13 @@ __global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
       pad_off[E] = xp + (p0 + p1) * kRowBlock;
       chunk_off[E] = xc + p0 + p1;
     }
-    if (otab) store_mixed_tables(E, c0, c1, p0, p1, xp, wsum, otab);
+  }
+  // one block past the routing blocks writes the mixed-order tables (a
+  // block without tokens, so no routing block waits for it); it has no
+  // slots or rows and ends here
+  if (otab && blockIdx.x == gridDim.x - 1) {
+    store_mixed_tables(E, c0, c1, p0, p1, xp, wsum, otab);
+    return;
   }
   __syncthreads();
 
@@ -289,10 +295,11 @@ __global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
   //    of earlier tokens (the K experts of one token are distinct), and after
   //    the earlier blocks' slots (prefix)
   const int nslot = ntok * K;
-  if (threadIdx.x < nslot) s_e[threadIdx.x] = ids[static_cast<int64_t>(tok0) * K + threadIdx.x];
+  const int tid = static_cast<int>(threadIdx.x);
+  if (tid < nslot) s_e[tid] = ids[static_cast<int64_t>(tok0) * K + tid];
   __syncthreads();
-  if (threadIdx.x < nslot) {
-    const int j = threadIdx.x;
+  if (tid < nslot) {
+    const int j = tid;
     const int e = s_e[j];
     int r = prefix[static_cast<int64_t>(blockIdx.x) * E + e];
     for (int j2 = 0; j2 < j - j % K; ++j2) r += s_e[j2] == e;
@@ -586,7 +593,10 @@ __global__ void debug_rows_kernel(int fmt, const int32_t* __restrict__ offsets,
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* w,
                          int32_t* blockhist, cudaStream_t s) {
   const int nb = (T + kTokensPerRouteBlock - 1) / kTokensPerRouteBlock;
-  auto k = E <= 128 ? route_kernel<4> : E <= 256 ? route_kernel<8> : route_kernel<16>;
+  auto k = E <= 128   ? route_kernel<4>
+           : E <= 256 ? route_kernel<8>
+           : E <= 384 ? route_kernel<12>
+                      : route_kernel<16>;
   return launch_pdl(g_pdl_small, k, dim3(nb), dim3(256), 0, s, logits, T, E, K, ids, w,
                     blockhist);
 }
@@ -616,8 +626,9 @@ cudaError_t launch_scatter_quant(int fmt, const int32_t* ids, int T, int E, int 
   const int threads = fmt == kFmtBF16    ? scatter_threads<kFmtBF16>()
                       : fmt == kFmtMXFP8 ? scatter_threads<kFmtMXFP8>()
                                          : scatter_threads<kFmtNVFP4>();
-  return launch_pdl(g_pdl_small, k, dim3(nb), dim3(threads), 0, s, ids, T, E, K, hb, H, prefix,
-                    counts, offsets, pad_off, chunk_off, perm, inv, prow_slot, otab, xq, xsf);
+  return launch_pdl(g_pdl_small, k, dim3(nb + (otab ? 1 : 0)), dim3(threads), 0, s, ids, T, E, K,
+                    hb, H, prefix, counts, offsets, pad_off, chunk_off, perm, inv, prow_slot, otab,
+                    xq, xsf);
 }
 
 cudaError_t launch_small_front(int fmt, const float* logits, int T, int E, int K,
