@@ -248,6 +248,23 @@ __global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok0 = blockIdx.x * kTokensPerRouteBlock;
   const int ntok = min(kTokensPerRouteBlock, T - tok0);
+  const int nslot = ntok * K;
+  const int tid = static_cast<int>(threadIdx.x);
+  const int tok = warp / W, part = warp % W;
+
+  // Loads that do not depend on the scans go out first, so their latency
+  // overlaps the scan: each slot's expert and its block prefix, and the
+  // first unit of this thread's share of its token row.
+  int slot_e = 0, slot_pre = 0;
+  if (tid < nslot) {
+    slot_e = ids[static_cast<int64_t>(tok0) * K + tid];
+    s_e[tid] = slot_e;
+    slot_pre = prefix[static_cast<int64_t>(blockIdx.x) * E + slot_e];
+  }
+  const __nv_bfloat16* xrow = hidden + static_cast<int64_t>(tok0 + tok) * H;
+  const int first = part * 32 + lane;
+  RawUnit<FMT> unit0;
+  if (tok < ntok && first < row_units<FMT>(H)) load_unit<FMT>(xrow, first, unit0);
 
   // 1. offsets
   const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
@@ -284,24 +301,20 @@ __global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
   // one block past the routing blocks writes the mixed-order tables (a
   // block without tokens, so no routing block waits for it); it has no
   // slots or rows and ends here
-  if (otab && blockIdx.x == gridDim.x - 1) {
+  if (otab && tok0 >= T) {
     store_mixed_tables(E, c0, c1, p0, p1, xp, wsum, otab);
     return;
   }
-  __syncthreads();
+  __syncthreads();  // s_off, s_poff and s_e are complete
 
   // 2. stable ranks, all of the block's slots at once: slot j = i*K + k
   //    ranks after the block's earlier slots of its expert, which are those
   //    of earlier tokens (the K experts of one token are distinct), and after
   //    the earlier blocks' slots (prefix)
-  const int nslot = ntok * K;
-  const int tid = static_cast<int>(threadIdx.x);
-  if (tid < nslot) s_e[tid] = ids[static_cast<int64_t>(tok0) * K + tid];
-  __syncthreads();
   if (tid < nslot) {
     const int j = tid;
-    const int e = s_e[j];
-    int r = prefix[static_cast<int64_t>(blockIdx.x) * E + e];
+    const int e = slot_e;
+    int r = slot_pre;
     for (int j2 = 0; j2 < j - j % K; ++j2) r += s_e[j2] == e;
     const int64_t s = static_cast<int64_t>(tok0) * K + j;
     perm[s_off[e] + r] = static_cast<int32_t>(s);
@@ -313,10 +326,8 @@ __global__ void __launch_bounds__(scatter_threads<FMT>()) scatter_quant_kernel(
   __syncthreads();
 
   // 3. GEMM1 input rows
-  const int tok = warp / W, part = warp % W;
   if (tok >= ntok) return;
-  quant_row_to_rows<FMT>(hidden + static_cast<int64_t>(tok0 + tok) * H, H, RowDsts{s_dst + tok * K},
-                         K, xq, xsf, part * 32 + lane, 32 * W);
+  quant_row_to_rows<FMT>(xrow, H, RowDsts{s_dst + tok * K}, K, xq, xsf, first, 32 * W, &unit0);
 }
 
 // ---------------------------------------------------------------- small batches

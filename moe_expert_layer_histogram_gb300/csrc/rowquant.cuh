@@ -145,17 +145,20 @@ __device__ __forceinline__ void quant_unit_to_rows(const __nv_bfloat16* __restri
 // takes units first, first + stride, ... (one warp: first = lane, stride
 // 32).  The next unit's load is issued before the current one is quantised
 // and stored, so each thread keeps two loads in flight instead of waiting out
-// the latency of every one.
+// the latency of every one.  loaded: unit `first`, already loaded by the
+// caller (or null).
 template <int FMT, class Dst>
 __device__ __forceinline__ void quant_row_to_rows(const __nv_bfloat16* __restrict__ x, int H,
                                                   const Dst& dst, int n,
                                                   uint8_t* __restrict__ xq,
                                                   uint8_t* __restrict__ xsf, int first,
-                                                  int stride = 32) {
+                                                  int stride = 32,
+                                                  const RawUnit<FMT>* loaded = nullptr) {
   const int U = row_units<FMT>(H);
   if (first >= U) return;
   RawUnit<FMT> cur;
-  load_unit<FMT>(x, first, cur);
+  if (loaded) cur = *loaded;
+  else load_unit<FMT>(x, first, cur);
   for (int u = first; u < U; u += stride) {
     RawUnit<FMT> nxt;
     const bool more = u + stride < U;
