@@ -279,7 +279,9 @@ cudaError_t launch_wide_or_pair(moe_layer* L, int epi, const GemmMaps& maps, con
     return launch_gemm_pair(epi, maps, a, clusters, s);
   }
   const int grid = static_cast<int>(std::min<int64_t>(L->max_ctas, chunks * a.n_tiles));
-  return launch_gemm(L->fmt, epi, maps, a, grid, max_rows, wide, s);
+  // GEMM2 with the fused combine has a kernel of its own (epilogue kind 4)
+  return launch_gemm(L->fmt, epi == 2 && a.gather_inv && wide ? 4 : epi, maps, a, grid, max_rows,
+                     wide, s);
 }
 
 // max_rows bounds the rows of any expert (selects the activation tile height).
@@ -647,7 +649,7 @@ moe_status forward_impl(moe_layer* L, const void* hidden, const float* logits, v
   const int pair = L->pair_scale_copies && T <= kPairCopyMaxTokens;
   // the fused combine runs in wide (prefill) GEMM2 launches only; narrower
   // launches keep the combine kernel (their GEMM2 kernels carry no gather)
-  const bool fused_combine = L->combine == MOE_COMBINE_FUSED && wide;
+  const bool fused_combine = L->combine == MOE_COMBINE_FUSED && wide && H % 256 == 0;
   void* reduce_out = L->combine == MOE_COMBINE_REDUCE || fused_combine ? out : nullptr;
   // decode: both GEMMs in one launch (for larger T the split measured faster)
   if (before_out && reduce_out) cudaStreamWaitEvent(s, before_out, 0);  // GEMM2 writes out
@@ -659,7 +661,7 @@ moe_status forward_impl(moe_layer* L, const void* hidden, const float* logits, v
   } else {
     if (e == cudaSuccess) e = run_gemm1(L, chunks, T, pair, wide, s, mixed);
     mark(4);
-    if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, wide, L->y, 0, s, out, mixed);
+    if (e == cudaSuccess) e = run_gemm2(L, chunks, T, pair, wide, L->y, 0, s, reduce_out, mixed);
   }
   mark(5);
   // with the in-kernel reduce or the fused combine GEMM2 has written `out` already

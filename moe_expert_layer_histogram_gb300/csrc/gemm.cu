@@ -698,7 +698,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT, NW), 1)
           uint32_t carry[5];
           epilogue_round<FMT, EPI>(v, 0, r < it.rows, prow, orow, n128, A, carry);
           epilogue_round<FMT, EPI>(v + 64, 1, r < it.rows, prow, orow, n128, A, carry);
-          if (EPI == 2 && A.gather_inv) combine_fused(r < it.rows, prow, n128, A);
+          if (EPI == 4 && A.gather_inv) combine_fused(r < it.rows, prow, n128, A);
         }
       }
     }
@@ -760,6 +760,7 @@ cudaError_t prepare_one() {
   if (e == cudaSuccess) e = prepare_m<FMT, 64, 1>();
   if (e == cudaSuccess) e = prepare_m<FMT, 128, 1>();
   if (e == cudaSuccess) e = prepare_m<FMT, 128, 2>();
+  if (e == cudaSuccess) e = set_smem<FMT, 4, 128, 2>();
   if (e == cudaSuccess) e = set_smem<FMT, 1, 32, 1, true>();
   if (e == cudaSuccess) e = set_smem<FMT, 3, 32, 1, true>();
   return e;
@@ -774,9 +775,15 @@ cudaError_t launch_fmt(const GemmMaps& maps, const GemmArgs& args, int grid, int
   return launch_one<FMT, EPI, 128, 1>(maps, args, maps, args, grid, s);
 }
 
+// epi 4: GEMM2 with the fused combine (wide launches only).  Its gather is
+// compiled into its own kernel: inside the plain GEMM2 kernel it made the
+// register allocator spill 172 bytes for every wide GEMM2 launch.
 template <int FMT>
 cudaError_t launch_epi(int epi, const GemmMaps& maps, const GemmArgs& args, int grid, int mrows,
                        bool wide, cudaStream_t s) {
+  if (epi == 4)
+    return wide ? launch_one<FMT, 4, 128, 2>(maps, args, maps, args, grid, s)
+                : cudaErrorInvalidValue;
   return epi == 1   ? launch_fmt<FMT, 1>(maps, args, grid, mrows, wide, s)
          : epi == 3 ? launch_fmt<FMT, 3>(maps, args, grid, mrows, wide, s)
                     : launch_fmt<FMT, 2>(maps, args, grid, mrows, wide, s);

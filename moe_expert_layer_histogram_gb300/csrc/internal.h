@@ -129,7 +129,8 @@ cudaError_t gemm_prepare(int fmt);  // raise the dynamic shared-memory limit
 // max_rows: upper bound on the rows of any expert in this launch (<= T);
 // selects the activation-tile height of the shared-memory stages.
 // epi: 1 = GEMM1 + SwiGLU, 3 = GEMM1 + ReLU^2 (both re-quantise into the
-// GEMM2 input format), 2 = GEMM2 (bf16 out).  wide: items of two 128-row
+// GEMM2 input format), 2 = GEMM2 (bf16 out), 4 = GEMM2 with the fused
+// combine (args.gather_inv; wide launches only).  wide: items of two 128-row
 // weight tiles (MMA N = 256; args.n_tiles counts those pairs), for launches
 // whose chunks are mostly full 128-row blocks.
 cudaError_t launch_gemm(int fmt, int epi, const GemmMaps& maps, const GemmArgs& args, int grid,
