@@ -87,7 +87,8 @@ typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_RELU2 = 1 } moe_activation;
  * result (bit-identical to GATHER), so no combine kernel runs (the combine
  * folded into the expert GEMM, as the MegaMoE kernel fuses its FC2 with the
  * reduction, sec. 六; here without atomics on the output).  Only
- * prefill-sized launches (T > 1024, the 256-column GEMM items) fuse it;
+ * prefill-sized launches (T > 1024 and H a multiple of 256: the 256-column
+ * GEMM2 items) fuse it;
  * smaller ones run the combine kernel (T <= 16: the single-launch decode
  * kernel's own combine), so their GEMM kernels carry no gather.  Measured
  * slower than GATHER on GB300 (the gathers lengthen GEMM2's epilogue).     */
