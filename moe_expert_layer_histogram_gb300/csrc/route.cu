@@ -508,6 +508,12 @@ __global__ void __launch_bounds__(256) batched_quant_kernel(
 // out[t] = bf16( sum_k w[t,k] * y[row(t,k)] ), fp32 accumulation in k order.
 // Grid (T, H/1024): each thread owns 8 consecutive columns (16-byte loads and
 // stores, coalesced along H).
+// kGroup rows' loads are in flight before their sums (which still run in k
+// order): 8 for prefill-sized launches (171 -> 165 us at T = 8192, 95 % of
+// the copy bandwidth), 1 for smaller ones, where the kernel launches early
+// behind GEMM2 (programmatic dependent launch) and its 64 registers per
+// thread instead of 32 cost the bf16 T = 512 layer 3 %.
+template <int kGroup>
 __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ y,
                                                       const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int K, int H,
@@ -527,15 +533,22 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
   float acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-  for (int k = 0; k < K; ++k) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(y + s_row[k] * H) + c);
-    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-    const float wk = s_w[k];
+  for (int k0 = 0; k0 < K; k0 += kGroup) {
+    uint4 u[kGroup];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
-      acc[2 * q] = fmaf(wk, p.x, acc[2 * q]);
-      acc[2 * q + 1] = fmaf(wk, p.y, acc[2 * q + 1]);
+    for (int i = 0; i < kGroup; ++i)
+      if (k0 + i < K) u[i] = __ldg(reinterpret_cast<const uint4*>(y + s_row[k0 + i] * H) + c);
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) {
+      if (k0 + i >= K) break;
+      const uint32_t wv[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+      const float wk = s_w[k0 + i];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+        acc[2 * q] = fmaf(wk, p.x, acc[2 * q]);
+        acc[2 * q + 1] = fmaf(wk, p.y, acc[2 * q + 1]);
+      }
     }
   }
   uint32_t o[4];
@@ -679,7 +692,8 @@ cudaError_t launch_batched_quant(int fmt, const void* hidden, const int32_t* cou
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int K, int H,
                            void* out, cudaStream_t s) {
   const dim3 grid(T, (H / 8 + 127) / 128);
-  return launch_pdl(g_pdl_small, combine_kernel, grid, dim3(128), 0, s,
+  auto k = T > 1024 ? combine_kernel<8> : combine_kernel<1>;
+  return launch_pdl(g_pdl_small, k, grid, dim3(128), 0, s,
                     static_cast<const __nv_bfloat16*>(y), inv, w, K, H,
                     static_cast<__nv_bfloat16*>(out));
 }
